@@ -1,0 +1,424 @@
+"""Benchmark of the Muon optimizer step on GB300 (one JSON line on stdout).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME]
+
+A step is one muon_step over every parameter of the workload (momentum,
+normalisation, 5 Newton-Schulz steps, weight-decay update).  The default
+workload is 74 separate bf16 [24, 10240] parameters grouped into one
+[74, 24, 10240] batch (the small-parameter case of the HyperParallel FSDP
+Muon RFC, section 3).  Inputs are seeded synthetic tensors generated on the
+device.  L2 is flushed (512 MB write) before every timed step; each step is
+timed with CUDA events on the launching stream and ms_per_step is their
+mean, max over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores on the same
+workload (a bounded sample of slices per step) and prints the same line
+with "impl": "reference".  Under torchrun only rank 0 runs it.
+
+With N > 1 (torchrun) each rank runs its own replica of the workload on its
+own GPU: slices are independent, there is no data-path collective
+("scaling": "weak"); a barrier brackets the timed region and the time is the
+max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "muon_step_matrices_per_s"
+UNIT = "matrices/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], tc=d["bf16_tflops"], tc_sustained=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sustained=1700.0, src="fallback")
+
+
+def workload_work(w):
+    """Algorithmic bytes (optimizer state touched once) and NS flops per step."""
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    per_el = es + 8 + 2 * es            # G read, M read+write, W read+write
+    nbytes = 0
+    flops = 0
+    skinny_bytes = 0
+    for s in w.shapes:
+        E, M, N = (s if len(s) == 3 else (1,) + tuple(s))
+        m, n = min(M, N), max(M, N)
+        nbytes += E * M * N * per_el
+        flops += E * w.ns_steps * (4 * m * m * n + 2 * m ** 3)
+        if m <= 64:
+            skinny_bytes += E * M * N * per_el
+    return nbytes, flops, skinny_bytes, per_el
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.t0 = time.time()
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def wait_first(self, timeout=5.0):
+        t = time.time()
+        while self.p is not None and time.time() - t < timeout:
+            self.f.flush()
+            if os.path.getsize(self.f.name) > 0:
+                return
+            time.sleep(0.05)
+
+    def stop(self):
+        if self.p is not None:
+            time.sleep(0.25)
+            self.p.terminate()
+            try:
+                self.p.wait(2)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, col in (("hw_slowdown", 5), ("hw_thermal_slowdown", 6),
+                              ("sw_thermal_slowdown", 7), ("sw_power_cap", 8)):
+                if r[col].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def skinny_traffic(per_launch_units):
+    """DRAM bytes of one fused-kernel launch from the committed ncu summary,
+    valid only while the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "skinny_kernel_74x24x10240.txt")
+    src = os.path.join(ROOT, "newton_schulz_05_gb300", "csrc", "skinny.cu")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    kv = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("skinny.cu sha256") != sha or "dram bytes per launch" not in kv:
+        return None
+    return float(kv["dram bytes per launch"])
+
+
+# ---------------------------------------------------------------- oracle leg
+def oracle_rate(w, budget_s: float, threads: int):
+    """Time the fp64 oracle on slices of the workload for about budget_s
+    seconds.  Returns (matrices/s for the whole workload, sample text)."""
+    import oracle
+
+    oracle.build()
+    shapes = list(w.shapes)
+    per_group = {}
+    for i, s in enumerate(shapes):
+        E, M, N = (s if len(s) == 3 else (1,) + tuple(s))
+        per_group.setdefault((M, N), [0, i])[0] += E
+    total_slices = sum(c for c, _ in per_group.values())
+    t_total = 0.0
+    notes = []
+    t_start = time.time()
+    for (M, N), (count, pidx) in per_group.items():
+        m, n = min(M, N), max(M, N)
+        fl = w.ns_steps * (4 * m * m * n + 2 * m ** 3)
+        # slices timed for this group: as many as fit the budget share, at least 1
+        W = synth.draw((M, N), w.param_std, synth.param_seed(1, pidx), w.dtype)
+        G = synth.draw((M, N), w.grad_std, synth.param_seed(0, pidx), w.dtype)
+        Mo = torch.zeros((M, N), dtype=torch.float32)
+        if fl > 50e9:
+            # a single slice would exceed the budget: time T=1 and scale by flops
+            t0 = time.time()
+            oracle.muon_slice(W, G, Mo, w.lr, w.beta, w.wd, w.nesterov, T=1, coeffs=w.coeffs,
+                              threads=threads)
+            dt = time.time() - t0
+            fl1 = 4 * m * m * n + 2 * m ** 3
+            t_slice = dt * fl / fl1
+            notes.append("%dx%d: 1 slice, 1 NS step, scaled by flops" % (M, N))
+        else:
+            k = max(1, min(count, threads))
+            t0 = time.time()
+            reps = 0
+            while True:
+                oracle.muon_slices([W] * k, [G] * k, [Mo] * k, w.lr, w.beta, w.wd, w.nesterov,
+                                   T=w.ns_steps, coeffs=w.coeffs, threads=threads, want_O=False)
+                reps += 1
+                if time.time() - t0 > budget_s / len(per_group):
+                    break
+            t_slice = (time.time() - t0) / (reps * k)
+            notes.append("%dx%d: %d slices" % (M, N, reps * k))
+        t_total += t_slice * count
+    rate = total_slices / t_total
+    return rate, "; ".join(notes), time.time() - t_start
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    import oracle
+
+    oracle.build()
+    # each step: the oracle over a bounded sample of the workload's slices
+    slices = []
+    for i, s in enumerate(w.shapes):
+        E, M, N = (s if len(s) == 3 else (1,) + tuple(s))
+        for e in range(E):
+            slices.append((i, M, N))
+    budget_per_step = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    # probe one slice to size the sample
+    i, M, N = slices[0]
+    W = synth.draw((M, N), w.param_std, synth.param_seed(1, i), w.dtype)
+    G = synth.draw((M, N), w.grad_std, synth.param_seed(0, i), w.dtype)
+    Mo = torch.zeros((M, N), dtype=torch.float32)
+    big = max(min(Mx, Nx) ** 2 * max(Mx, Nx) for _, Mx, Nx in slices) > 2e10
+    if big:
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "the fp64 oracle needs minutes per slice of this workload; "
+                          "the reference arm runs on the skinny workloads only"}))
+        return
+    t0 = time.time()
+    oracle.muon_slices([W] * threads, [G] * threads, [Mo] * threads, w.lr, w.beta, w.wd,
+                       w.nesterov, T=w.ns_steps, coeffs=w.coeffs, threads=threads, want_O=False)
+    per_round = time.time() - t0
+    rounds = max(1, int(budget_per_step / per_round))
+    k = min(len(slices), rounds * threads)
+    Ws = [W] * k; Gs = [G] * k; Ms = [Mo] * k
+    times = []
+    for it in range(args.warmup + args.steps):
+        t0 = time.time()
+        oracle.muon_slices(Ws, Gs, Ms, w.lr, w.beta, w.wd, w.nesterov, T=w.ns_steps,
+                           coeffs=w.coeffs, threads=threads, want_O=False)
+        if it >= args.warmup:
+            times.append(time.time() - t0)
+    t = sum(times) / len(times)
+    rate = k / t
+    ms_step = 1e3 * len(slices) / rate
+    sample = "%d of %d slices per step (%dx%d), fp64 oracle, %d threads" % (
+        k, len(slices), M, N, threads)
+    out = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": w.name, "slices": len(slices)},
+           "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import newton_schulz_05_gb300 as mu
+    from newton_schulz_05_gb300 import build as mb
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        mb.build()
+    if ws_n > 1:
+        dist.barrier()
+    mb.build()
+    mu.load()
+
+    shapes = list(w.shapes)
+    plan = mu.Plan(list(zip(shapes, [w.dtype] * len(shapes))))
+    W = synth.make_params(w, device=dev)
+    G = synth.make_grads(w, 0, device=dev)
+    M = synth.make_momentum(w, device=dev)
+    wsp = mu.alloc_workspace(plan, dev)
+    stream = torch.cuda.current_stream(dev)
+    hp = dict(lr=w.lr, beta=w.beta, wd=w.wd, nesterov=w.nesterov, ns_steps=w.ns_steps,
+              coeffs=w.coeffs)
+    step = mu.PreparedStep(plan, W, G, M, workspace=wsp, stream=stream, **hp)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches_per_step = plan.launches(w.ns_steps)
+    n_slices = plan.num_slices
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    assert mu.workspace_error(wsp, stream) == 0
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.wait_first()
+    if ws_n > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall = time.time()
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.time() - t_wall
+    if ws_n > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(per) / len(per)
+    if ws_n > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    err = mu.workspace_error(wsp, stream)
+
+    # ---- end to end through the public API, host buffers (pinned)
+    Wh = [x.cpu().pin_memory() for x in W]
+    Gh = [x.cpu().pin_memory() for x in G]
+    Mh = [x.cpu().pin_memory() for x in M]
+    h2d = sum(x.numel() * x.element_size() for x in Wh + Gh + Mh)
+    d2h = sum(x.numel() * x.element_size() for x in Wh + Mh)
+    Wd = [torch.empty_like(x, device=dev) for x in Wh]
+    Gd = [torch.empty_like(x, device=dev) for x in Gh]
+    Md = [torch.empty_like(x, device=dev) for x in Mh]
+    opt_step = mu.PreparedStep(plan, Wd, Gd, Md, workspace=wsp, stream=stream, **hp)
+
+    def e2e_step():
+        for d, h in zip(Wd + Gd + Md, Wh + Gh + Mh):
+            d.copy_(h, non_blocking=True)
+        opt_step()
+        for d, h in zip(Wd + Md, Wh + Mh):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(min(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(1, min(args.steps, 50))
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1) / e_steps
+    if ws_n > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    nbytes, flops, skinny_bytes, per_el = workload_work(w)
+    pk = peaks()
+    kinds = {g["kernel"] for g in plan.groups()}
+    if kinds == {mu.KERNEL_SKINNY} and launches_per_step == 1:
+        # one fused launch per step: its duration is the step's event time
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        traffic = skinny_traffic(n_slices)
+        roof = {"bound": "hbm", "kernel": "skinny_kernel", "achieved": achieved,
+                "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
+                "traffic": traffic,
+                "note": "algorithmic bytes %d B/element x %d elements per launch; peak %s" % (
+                    per_el, w.num_elements, "of measured" if pk["src"] == "measured" else "of fallback")}
+    else:
+        achieved = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "whole step", "achieved": achieved,
+                "peak": pk["tc"], "unit": "TFLOP/s", "frac": achieved / pk["tc"], "traffic": None,
+                "note": "standard NS flops over the whole step; peak bf16 burst %s" % (
+                    "of measured" if pk["src"] == "measured" else "of fallback")}
+
+    out = {"metric": METRIC, "value": n_slices * ws_n / (ms * 1e-3), "unit": UNIT,
+           "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f16", "data": "synthetic",
+           "config": {"workload": w.name, "slices": n_slices, "param_dtype": str(w.dtype),
+                      "ns_steps": w.ns_steps, "l2": "flushed (512 MB write) before each timed step",
+                      "parallelism": "replica per GPU" if ws_n > 1 else "single GPU",
+                      "mode": "fp16 tensor-core operands, fp32 accumulate"},
+           "roofline": roof,
+           "e2e": {"value": n_slices * ws_n / (ms_e2e * 1e-3), "unit": UNIT,
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+           "clocks": clocks, "gpu_launches": launches_per_step * args.steps,
+           "wall_s_timed": t_wall, "device_error": err}
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        rate, sample, used = oracle_rate(w, budget_s=15.0, threads=os.cpu_count() or 1)
+        out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count() or 1,
+                               "kind": "oracle", "sample": sample + " (%.1f s)" % used}
+    if rank == 0:
+        print(json.dumps(out))
+    if ws_n > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="skinny_74x24x10240", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = synth.workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

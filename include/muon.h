@@ -1,0 +1,176 @@
+/*
+ * libmuon: the Muon optimizer step on one GB300 (sm_103a), C ABI.
+ *
+ * The step (HyperParallel FSDP Muon RFC, mindspore hyper-parallel issue
+ * "HyperParallel FSDP Muon优化器性能优化 RFC"):
+ *   1. momentum   M' = beta*M + G;  V = G + beta*M' (Nesterov) or V = M'
+ *                 (section 1(1): the orthogonalised matrix is the gradient
+ *                 momentum M_t);
+ *   2. normalise  X0 = V / (||V||_F + eps) per matrix slice;
+ *   3. Newton-Schulz, T steps on the slice, worked on transposed when M > N
+ *                 (sections 1 and 2: needs the whole matrix, depends only on
+ *                 the last two dims):
+ *                   A = X X^T;  B = b*A + c*A*A;  X <- a*X + B*X;
+ *   4. update     W' = W*(1 - lr*wd) - lr*s*O,  s = sqrt(max(1, M/N))
+ *                 (section 6: AdamW-style decoupled weight decay).
+ * Slices whose trailing dims agree are regrouped into one batch and each
+ * [E, M, N] tensor contributes E independent slices (sections 2 and 3).
+ *
+ * Ownership: the caller allocates and owns every device buffer (parameters,
+ * gradients, momentum, workspace).  A plan owns host memory only.  muon_step
+ * is asynchronous on the given stream, allocates nothing and never
+ * synchronises the host.
+ *
+ * Errors: every call returns a muon_status; nothing aborts or throws.
+ * Arguments are validated before any launch.  Launch failures return
+ * MUON_ERR_CUDA.  A device-side wait that runs out of its iteration budget
+ * writes an error word into the workspace header; muon_workspace_error reads
+ * it.
+ */
+#ifndef MUON_H_
+#define MUON_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MUON_API __attribute__((visibility("default")))
+#else
+#define MUON_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MUON_OK = 0,
+  MUON_ERR_INVALID_ARG = -1,       /* null pointer, bad count, bad option   */
+  MUON_ERR_UNSUPPORTED_SHAPE = -2, /* ndim not in {2,3}, a zero dimension    */
+  MUON_ERR_DTYPE = -3,             /* dtype not MUON_BF16 / MUON_F32         */
+  MUON_ERR_ALIGNMENT = -4,         /* workspace not 256-byte aligned         */
+  MUON_ERR_CUDA = -5,              /* a CUDA runtime call failed             */
+  MUON_ERR_DEVICE_TIMEOUT = -6,    /* a bounded device wait gave up          */
+  MUON_ERR_WORKSPACE = -7          /* workspace smaller than the plan needs  */
+} muon_status;
+
+/* element types of parameters and gradients (momentum is always fp32) */
+enum { MUON_BF16 = 0, MUON_F32 = 1 };
+
+/* arithmetic of the Newton-Schulz products */
+enum {
+  /* fp16 tensor-core operands, fp32 accumulation; the iterates are
+   * normalised (spectral norm <= 1.21), so fp16 cannot overflow and carries
+   * three more mantissa bits than bf16 */
+  MUON_MODE_TC16 = 0,
+  /* fp32 operands and accumulation throughout (accuracy mode) */
+  MUON_MODE_FP32 = 1
+};
+
+/* which kernel family a group runs on (reported by muon_plan_group) */
+enum { MUON_KERNEL_SKINNY = 0, MUON_KERNEL_DENSE = 1 };
+
+/* One parameter: [M, N] (ndim 2) or [E, M, N] (ndim 3), row-major,
+ * contiguous.  dims[k] for k >= ndim is ignored. */
+typedef struct {
+  int ndim;
+  int64_t dims[3];
+  int dtype; /* MUON_BF16 or MUON_F32 */
+} muon_shape;
+
+typedef struct {
+  int mode;             /* MUON_MODE_TC16 (default) or MUON_MODE_FP32        */
+  float eps;            /* normalisation eps, default 1e-7                   */
+  size_t workspace_cap; /* bytes; 0 = no cap.  Dense groups are processed in
+                           chunks of slices that fit the cap; chunking never
+                           changes results (slices are independent).        */
+  int skinny_max_m;     /* groups with min(M,N) <= this run on the fused
+                           skinny kernel when they fit on chip (default 64,
+                           0 or negative disables the skinny kernel)        */
+} muon_options;
+
+typedef struct muon_plan_s muon_plan_t;
+
+typedef struct {
+  int64_t M, N;   /* slice dims as stored                                 */
+  int64_t m, n;   /* working dims: m = min(M,N), n = max(M,N)             */
+  int dtype;
+  int count;      /* slices in the group                                   */
+  int tr;         /* 1 when M > N: the slice is worked on transposed       */
+  float scale;    /* s = sqrt(max(1, M/N)), rounded once to float          */
+  int kernel;     /* MUON_KERNEL_SKINNY or MUON_KERNEL_DENSE               */
+  int cluster;    /* skinny: CTAs per slice (thread-block cluster size)    */
+  int chunk;      /* dense: slices per chunk under the workspace cap       */
+} muon_group_info;
+
+/* Fill *opt with the defaults listed above. */
+MUON_API void muon_options_default(muon_options* opt);
+
+/*
+ * Build a plan (host only; no device call).  RFC section 3: slices are
+ * grouped by key (M, N, dtype) in order of first appearance while walking
+ * parameters in call order and slices e = 0..E-1 within each; a slice's
+ * index in its group is its order of encounter.  shapes: n entries, host.
+ * opt may be null (defaults).  On success *out receives a plan to be freed
+ * with muon_plan_destroy.
+ */
+MUON_API muon_status muon_plan(const muon_shape* shapes, int n, const muon_options* opt,
+                      muon_plan_t** out);
+
+/* Device workspace bytes muon_step needs for this plan (>= 256). */
+MUON_API muon_status muon_plan_workspace_bytes(const muon_plan_t* plan, size_t* out);
+MUON_API muon_status muon_plan_num_groups(const muon_plan_t* plan, int* out);
+MUON_API muon_status muon_plan_num_slices(const muon_plan_t* plan, int* out);
+MUON_API muon_status muon_plan_group(const muon_plan_t* plan, int g, muon_group_info* out);
+/* group id and index within the group of slice `slice` of parameter `param` */
+MUON_API muon_status muon_plan_slice(const muon_plan_t* plan, int param, int slice,
+                            int* group, int* index);
+
+/*
+ * One Muon step for every parameter of the plan, enqueued on `stream`
+ * (a cudaStream_t; null = legacy default stream).
+ *   params[p]   device, dtype of shape p, updated in place (RNE rounding)
+ *   grads[p]    device, same dtype and shape, read only
+ *   momentum[p] device, fp32, same shape, updated in place
+ *   coeffs      host, 3 floats (a, b, c); null = (3.4445, -4.7750, 2.0315)
+ *   ns_steps    T >= 0
+ *   workspace   device, 256-byte aligned, >= muon_plan_workspace_bytes
+ * Parameter, gradient and momentum buffers must not overlap one another.
+ */
+MUON_API muon_status muon_step(const muon_plan_t* plan, void* const* params,
+                      const void* const* grads, float* const* momentum,
+                      float lr, float beta, float wd, int nesterov,
+                      int ns_steps, const float* coeffs, void* workspace,
+                      size_t ws_bytes, void* stream);
+
+/*
+ * muon_step that also writes the orthogonalised momentum O (fp32, the
+ * parameter's own shape and layout) of every slice into ortho[p], a device
+ * buffer per parameter.  Used to check O itself against a reference.
+ */
+MUON_API muon_status muon_step_ortho(const muon_plan_t* plan, void* const* params,
+                            const void* const* grads, float* const* momentum,
+                            float lr, float beta, float wd, int nesterov,
+                            int ns_steps, const float* coeffs, void* workspace,
+                            size_t ws_bytes, void* stream, float* const* ortho);
+
+/*
+ * Read the device error word of a workspace after synchronising `stream`.
+ * *code receives MUON_OK or the first device-side error recorded
+ * (MUON_ERR_DEVICE_TIMEOUT); when clear != 0 the word is reset to zero.
+ */
+MUON_API muon_status muon_workspace_error(const void* workspace, void* stream, int clear,
+                                 int* code);
+
+/* Kernel launches muon_step makes for this plan and ns_steps (for
+ * accounting; no device call). */
+MUON_API muon_status muon_plan_launches(const muon_plan_t* plan, int ns_steps, int* out);
+
+MUON_API void muon_plan_destroy(muon_plan_t* plan);
+MUON_API const char* muon_status_string(muon_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_H_ */

@@ -1,0 +1,312 @@
+"""Muon optimizer step on one GB300: thin Python binding of libmuon.
+
+Every step of the optimizer runs in libmuon's CUDA kernels (C ABI declared in
+include/muon.h); this module only marshals tensor pointers and the stream.
+PyTorch provides device memory and streams.  There is no CPU fallback: if
+libmuon.so is missing or cannot be loaded, importing the binding raises.
+
+The step (HyperParallel FSDP Muon RFC, mindspore hyper-parallel issue
+"HyperParallel FSDP Muon优化器性能优化 RFC", sections 1-3 and 6):
+momentum / Nesterov -> per-slice Frobenius normalisation -> quintic
+Newton-Schulz on min(M,N) x max(M,N) -> W' = W (1 - lr wd) - lr s O, with
+slices of equal trailing dims grouped into one batch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmuon.so")
+
+MUON_OK = 0
+MUON_BF16, MUON_F32 = 0, 1
+MODE_TC16, MODE_FP32 = 0, 1
+KERNEL_SKINNY, KERNEL_DENSE = 0, 1
+DEFAULT_COEFFS = (3.4445, -4.7750, 2.0315)
+
+_DTYPES = {torch.bfloat16: MUON_BF16, torch.float32: MUON_F32}
+_MODES = {"tc16": MODE_TC16, "fp32": MODE_FP32}
+
+
+class MuonError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("ndim", ctypes.c_int), ("dims", ctypes.c_int64 * 3), ("dtype", ctypes.c_int)]
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("eps", ctypes.c_float),
+                ("workspace_cap", ctypes.c_size_t), ("skinny_max_m", ctypes.c_int)]
+
+
+class _GroupInfo(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("m", ctypes.c_int64),
+                ("n", ctypes.c_int64), ("dtype", ctypes.c_int), ("count", ctypes.c_int),
+                ("tr", ctypes.c_int), ("scale", ctypes.c_float), ("kernel", ctypes.c_int),
+                ("cluster", ctypes.c_int), ("chunk", ctypes.c_int)]
+
+
+EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
+           "muon_plan_num_groups", "muon_plan_num_slices", "muon_plan_group",
+           "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
+           "muon_plan_launches", "muon_plan_destroy", "muon_status_string"]
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libmuon.so (built by newton_schulz_05_gb300.build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libmuon.so not built at %s: run newton_schulz_05_gb300.build.build() "
+                           "(there is no CPU fallback)" % path)
+    L = ctypes.CDLL(path)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    L.muon_options_default.argtypes = [ctypes.POINTER(_Options)]
+    L.muon_options_default.restype = None
+    L.muon_plan.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, ctypes.POINTER(_Options), PP]
+    L.muon_plan_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
+    L.muon_plan_num_groups.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+    L.muon_plan_num_slices.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+    L.muon_plan_group.argtypes = [vp, ctypes.c_int, ctypes.POINTER(_GroupInfo)]
+    L.muon_plan_slice.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                  ctypes.POINTER(ctypes.c_int)]
+    step_args = [vp, PP, PP, PP, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_int,
+                 ctypes.c_int, ctypes.POINTER(ctypes.c_float), vp, sz, vp]
+    L.muon_step.argtypes = step_args
+    L.muon_step_ortho.argtypes = step_args + [PP]
+    L.muon_workspace_error.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    L.muon_plan_launches.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    L.muon_plan_destroy.argtypes = [vp]
+    L.muon_plan_destroy.restype = None
+    L.muon_status_string.argtypes = [ctypes.c_int]
+    L.muon_status_string.restype = ctypes.c_char_p
+    for fn in ("muon_plan", "muon_plan_workspace_bytes", "muon_plan_num_groups",
+               "muon_plan_num_slices", "muon_plan_group", "muon_plan_slice", "muon_step",
+               "muon_step_ortho", "muon_workspace_error", "muon_plan_launches"):
+        getattr(L, fn).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(s: int) -> str:
+    return load().muon_status_string(s).decode()
+
+
+def _check(status: int, what: str):
+    if status != MUON_OK:
+        raise MuonError(status, what)
+
+
+def _shape_of(t) -> Tuple[Tuple[int, ...], int]:
+    if isinstance(t, torch.Tensor):
+        if t.dtype not in _DTYPES:
+            raise TypeError("parameters must be bf16 or fp32, got %s" % t.dtype)
+        return tuple(t.shape), _DTYPES[t.dtype]
+    shape, dtype = t
+    return tuple(shape), _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+
+
+class Plan:
+    """Host-side grouping of parameters by trailing dims (muon_plan)."""
+
+    def __init__(self, params: Sequence, mode: str = "tc16", eps: float = 1e-7,
+                 workspace_cap: int = 0, skinny_max_m: int = 64):
+        L = load()
+        specs = [_shape_of(p) for p in params]
+        n = len(specs)
+        arr = (_Shape * max(n, 1))()
+        for i, (shape, dt) in enumerate(specs):
+            arr[i].ndim = len(shape)
+            for k in range(min(len(shape), 3)):
+                arr[i].dims[k] = shape[k]
+            arr[i].dtype = dt
+        opt = _Options()
+        L.muon_options_default(ctypes.byref(opt))
+        opt.mode = _MODES[mode]
+        opt.eps = eps
+        opt.workspace_cap = workspace_cap
+        opt.skinny_max_m = skinny_max_m
+        h = ctypes.c_void_p()
+        _check(L.muon_plan(arr, n, ctypes.byref(opt), ctypes.byref(h)), "muon_plan")
+        self._h = h
+        self.shapes = [s for s, _ in specs]
+        self.dtypes = [d for _, d in specs]
+        self.mode = mode
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib is not None:
+            _lib.muon_plan_destroy(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def workspace_bytes(self) -> int:
+        v = ctypes.c_size_t()
+        _check(load().muon_plan_workspace_bytes(self._h, ctypes.byref(v)), "workspace_bytes")
+        return v.value
+
+    @property
+    def num_slices(self) -> int:
+        v = ctypes.c_int()
+        _check(load().muon_plan_num_slices(self._h, ctypes.byref(v)), "num_slices")
+        return v.value
+
+    def groups(self) -> List[dict]:
+        L = load()
+        n = ctypes.c_int()
+        _check(L.muon_plan_num_groups(self._h, ctypes.byref(n)), "num_groups")
+        out = []
+        for g in range(n.value):
+            gi = _GroupInfo()
+            _check(L.muon_plan_group(self._h, g, ctypes.byref(gi)), "plan_group")
+            out.append({f: getattr(gi, f) for f, _ in _GroupInfo._fields_})
+        return out
+
+    def slice(self, param: int, e: int) -> Tuple[int, int]:
+        g, i = ctypes.c_int(), ctypes.c_int()
+        _check(load().muon_plan_slice(self._h, param, e, ctypes.byref(g), ctypes.byref(i)),
+               "plan_slice")
+        return g.value, i.value
+
+    def launches(self, ns_steps: int = 5) -> int:
+        v = ctypes.c_int()
+        _check(load().muon_plan_launches(self._h, ns_steps, ctypes.byref(v)), "plan_launches")
+        return v.value
+
+
+def _ptrs(ts) -> ctypes.Array:
+    return (ctypes.c_void_p * max(len(ts), 1))(*[t.data_ptr() for t in ts])
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def step(plan: Plan, params, grads, momentum, *, lr: float, beta: float, wd: float,
+         nesterov: bool = True, ns_steps: int = 5, coeffs=DEFAULT_COEFFS,
+         workspace: torch.Tensor, stream=None, ortho=None) -> None:
+    """Enqueue one Muon step (muon_step / muon_step_ortho) on `stream`.
+
+    params / grads / momentum: lists of contiguous CUDA tensors in plan order;
+    momentum is fp32.  ortho (optional): fp32 tensors shaped like params that
+    receive the orthogonalised momentum O."""
+    L = load()
+    n = len(plan.shapes)
+    if not (len(params) == len(grads) == len(momentum) == n):
+        raise ValueError("expected %d params, grads and momentum tensors" % n)
+    for i, (p, g, m) in enumerate(zip(params, grads, momentum)):
+        if tuple(p.shape) != plan.shapes[i] or tuple(g.shape) != plan.shapes[i] or \
+                tuple(m.shape) != plan.shapes[i]:
+            raise ValueError("tensor %d does not match the plan's shape %s" % (i, plan.shapes[i]))
+        if _DTYPES.get(p.dtype) != plan.dtypes[i] or g.dtype != p.dtype or m.dtype != torch.float32:
+            raise TypeError("tensor %d: dtype mismatch with the plan" % i)
+        if not (p.is_cuda and g.is_cuda and m.is_cuda):
+            raise ValueError("tensor %d is not on a CUDA device" % i)
+        if not (p.is_contiguous() and g.is_contiguous() and m.is_contiguous()):
+            raise ValueError("tensor %d is not contiguous" % i)
+    c = (ctypes.c_float * 3)(*coeffs)
+    args = [plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum), lr, beta, wd,
+            int(bool(nesterov)), ns_steps, c, ctypes.c_void_p(workspace.data_ptr()),
+            workspace.numel() * workspace.element_size(), ctypes.c_void_p(_stream_handle(stream))]
+    if ortho is None:
+        _check(L.muon_step(*args), "muon_step")
+    else:
+        for i, o in enumerate(ortho):
+            if tuple(o.shape) != plan.shapes[i] or o.dtype != torch.float32 or not o.is_contiguous():
+                raise ValueError("ortho %d must be a contiguous fp32 tensor of the param's shape" % i)
+        _check(L.muon_step_ortho(*args, _ptrs(ortho)), "muon_step_ortho")
+
+
+def workspace_error(workspace: torch.Tensor, stream=None, clear: bool = True) -> int:
+    """Device error word of the workspace (synchronises the stream)."""
+    code = ctypes.c_int()
+    _check(load().muon_workspace_error(ctypes.c_void_p(workspace.data_ptr()),
+                                       ctypes.c_void_p(_stream_handle(stream)), int(clear),
+                                       ctypes.byref(code)), "workspace_error")
+    return code.value
+
+
+def alloc_workspace(plan: Plan, device=None) -> torch.Tensor:
+    """A zeroed device workspace of the plan's size (torch's allocator returns
+    256-byte aligned blocks)."""
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=device or "cuda")
+    if ws.data_ptr() % 256:
+        raise RuntimeError("workspace not 256-byte aligned")
+    return ws
+
+
+class Muon:
+    """Muon optimizer over a fixed list of parameter tensors.
+
+    Holds the plan, the fp32 momentum buffers and the workspace; ``step(grads)``
+    runs one optimizer step in place on the CUDA stream."""
+
+    def __init__(self, params: Sequence[torch.Tensor], lr: float = 0.02, beta: float = 0.95,
+                 wd: float = 0.1, nesterov: bool = True, ns_steps: int = 5,
+                 coeffs=DEFAULT_COEFFS, mode: str = "tc16", eps: float = 1e-7):
+        self.params = list(params)
+        self.plan = Plan(self.params, mode=mode, eps=eps)
+        self.momentum = [torch.zeros_like(p, dtype=torch.float32) for p in self.params]
+        self.workspace = alloc_workspace(self.plan, self.params[0].device if self.params else None)
+        self.hp = dict(lr=lr, beta=beta, wd=wd, nesterov=nesterov, ns_steps=ns_steps,
+                       coeffs=coeffs)
+
+    def step(self, grads: Sequence[torch.Tensor], stream=None) -> None:
+        step(self.plan, self.params, grads, self.momentum, workspace=self.workspace,
+             stream=stream, **self.hp)
+
+
+class PreparedStep:
+    """A muon_step call with its argument arrays marshalled once.
+
+    For a fixed set of tensors (the usual case: parameters, gradient buffers
+    and momentum never move) calling the object enqueues one step with a
+    single C call and no per-call Python-side validation."""
+
+    def __init__(self, plan: Plan, params, grads, momentum, *, lr: float, beta: float, wd: float,
+                 nesterov: bool = True, ns_steps: int = 5, coeffs=DEFAULT_COEFFS,
+                 workspace: torch.Tensor, stream=None, ortho=None):
+        # validate once through the checked path's rules
+        n = len(plan.shapes)
+        if not (len(params) == len(grads) == len(momentum) == n):
+            raise ValueError("expected %d params, grads and momentum tensors" % n)
+        for i, (p, g, m) in enumerate(zip(params, grads, momentum)):
+            if tuple(p.shape) != plan.shapes[i] or g.shape != p.shape or m.shape != p.shape:
+                raise ValueError("tensor %d does not match the plan's shape" % i)
+            if _DTYPES.get(p.dtype) != plan.dtypes[i] or g.dtype != p.dtype or m.dtype != torch.float32:
+                raise TypeError("tensor %d: dtype mismatch with the plan" % i)
+            if not (p.is_cuda and g.is_cuda and m.is_cuda and p.is_contiguous() and
+                    g.is_contiguous() and m.is_contiguous()):
+                raise ValueError("tensor %d must be a contiguous CUDA tensor" % i)
+        self._keep = (plan, list(params), list(grads), list(momentum), workspace, ortho)
+        self._fn = load().muon_step_ortho if ortho is not None else load().muon_step
+        c = (ctypes.c_float * 3)(*coeffs)
+        self._args = [plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum),
+                      ctypes.c_float(lr), ctypes.c_float(beta), ctypes.c_float(wd),
+                      ctypes.c_int(int(bool(nesterov))), ctypes.c_int(ns_steps), c,
+                      ctypes.c_void_p(workspace.data_ptr()),
+                      ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                      ctypes.c_void_p(_stream_handle(stream))]
+        if ortho is not None:
+            self._args.append(_ptrs(ortho))
+
+    def __call__(self) -> None:
+        _check(self._fn(*self._args), "muon_step")

@@ -1,0 +1,266 @@
+// Dense path of the Muon step: groups whose working matrix is too large for
+// the fused on-chip kernel.  Per chunk of slices of one group:
+//
+//   front      M' = beta*M + G;  V = G + beta*M' | M'  -> V (fp32, working
+//              layout [m_pad, n_pad], transposed when M > N), M' in place,
+//              per-tile partial sums of V^2               (HBM-bound)
+//   finalize   s = 1 / (sqrt(sum of partials) + eps) per slice
+//   normalize  X0 = s*V in the iterate type
+//   T x        A = X X^T;  B = b*A + c*A*A;  X <- a*X + B*X   (GEMMs)
+//   epilogue   W' = W*(1 - lr*wd) - lr*scale*O  in the parameter layout
+//
+// (HyperParallel FSDP Muon RFC, mindspore hyper-parallel issue
+// "HyperParallel FSDP Muon优化器性能优化 RFC": section 1(1) momentum input,
+// sections 2/3 batched slices, section 6 decoupled weight decay.)
+//
+// Working buffers are padded to multiples of 128 with zeros.  Zero rows and
+// columns stay exactly zero under the iteration (A, B and the update of a
+// zero row or column are zero), so padding changes no result.
+#include <cstdio>
+
+#include "common.cuh"
+#include "internal.h"
+#include "gemm.cuh"
+
+namespace muon {
+
+namespace {
+
+constexpr int kNT = 256;
+
+struct DenseBufs {
+  float* V;        // [m_pad, n_pad] fp32: front output, then O
+  void* X0;        // iterate ping
+  void* X1;        // iterate pong
+  void* A;         // [m_pad, m_pad]
+  void* B;         // [m_pad, m_pad]
+  float* part;     // front partial sums
+  float* inv;      // per-slice 1/(||V|| + eps)
+};
+
+template <typename PT>
+__global__ void __launch_bounds__(kNT) front_kernel(
+    const __grid_constant__ SlicePtrs ptrs, int64_t m, int64_t n, int64_t m_pad,
+    int64_t n_pad, int tr, float beta, int nesterov, char* ws, size_t slice_ws,
+    size_t off_V, size_t off_part) {
+  const int s = blockIdx.y;
+  const int tiles_c = (int)(n_pad / kFrontTileC);
+  const int64_t i0 = (int64_t)(blockIdx.x / tiles_c) * kFrontTileR;
+  const int64_t k0 = (int64_t)(blockIdx.x % tiles_c) * kFrontTileC;
+  char* base = ws + (size_t)s * slice_ws;
+  float* V = reinterpret_cast<float*>(base + off_V);
+  float* part = reinterpret_cast<float*>(base + off_part);
+  const PT* G = static_cast<const PT*>(ptrs.G[s]);
+  float* Mo = ptrs.Mom[s];
+  __shared__ float red[kNT / 32];
+  __shared__ float tile[kFrontTileC][kFrontTileR + 1];
+  float ss = 0.f;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (!tr) {
+    // working (i, k) = stored (i, k); stored slice is [m, n]
+    for (int r = warp; r < kFrontTileR; r += kNT / 32) {
+      const int64_t i = i0 + r;
+      for (int c = lane; c < kFrontTileC; c += 32) {
+        const int64_t k = k0 + c;
+        float v = 0.f;
+        if (i < m && k < n) {
+          const int64_t idx = i * n + k;
+          const float g = to_f(G[idx]);
+          const float mm = fmaf(beta, Mo[idx], g);
+          Mo[idx] = mm;
+          v = nesterov ? fmaf(beta, mm, g) : mm;
+        }
+        ss = fmaf(v, v, ss);
+        V[i * n_pad + k] = v;
+      }
+    }
+  } else {
+    // working (i, k) = stored (k, i); stored slice is [n, m]
+    for (int c = warp; c < kFrontTileC; c += kNT / 32) {
+      const int64_t k = k0 + c;
+      const int64_t i = i0 + lane;
+      float v = 0.f;
+      if (i < m && k < n) {
+        const int64_t idx = k * m + i;
+        const float g = to_f(G[idx]);
+        const float mm = fmaf(beta, Mo[idx], g);
+        Mo[idx] = mm;
+        v = nesterov ? fmaf(beta, mm, g) : mm;
+      }
+      ss = fmaf(v, v, ss);
+      tile[c][lane] = v;
+    }
+    __syncthreads();
+    for (int r = warp; r < kFrontTileR; r += kNT / 32)
+      for (int c = lane; c < kFrontTileC; c += 32) V[(i0 + r) * n_pad + k0 + c] = tile[c][r];
+  }
+  const float tot = block_sum<kNT>(ss, red);
+  if (threadIdx.x == 0) part[blockIdx.x] = tot;
+}
+
+__global__ void __launch_bounds__(kNT) finalize_kernel(char* ws, size_t slice_ws,
+                                                       size_t off_part, size_t off_inv,
+                                                       int nblk, float eps) {
+  char* base = ws + (size_t)blockIdx.x * slice_ws;
+  const float* part = reinterpret_cast<const float*>(base + off_part);
+  __shared__ float red[kNT / 32];
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < nblk; i += kNT) ss += part[i];
+  const float tot = block_sum<kNT>(ss, red);
+  if (threadIdx.x == 0) *reinterpret_cast<float*>(base + off_inv) = 1.f / (sqrtf(tot) + eps);
+}
+
+// X0 = s*V in the iterate type; with T == 0 the scaled V is O itself.
+template <typename IT>
+__global__ void __launch_bounds__(kNT) normalize_kernel(char* ws, size_t slice_ws,
+                                                        size_t off_V, size_t off_X,
+                                                        size_t off_inv, int64_t count,
+                                                        int in_place) {
+  char* base = ws + (size_t)blockIdx.y * slice_ws;
+  float* V = reinterpret_cast<float*>(base + off_V);
+  IT* X = reinterpret_cast<IT*>(base + off_X);
+  const float s = *reinterpret_cast<const float*>(base + off_inv);
+  const int64_t stride = (int64_t)gridDim.x * kNT * 4;
+  for (int64_t i = ((int64_t)blockIdx.x * kNT + threadIdx.x) * 4; i < count; i += stride) {
+    float4 v = *reinterpret_cast<const float4*>(V + i);
+    v.x *= s; v.y *= s; v.z *= s; v.w *= s;
+    if (in_place) {
+      *reinterpret_cast<float4*>(V + i) = v;
+    } else {
+      X[i + 0] = from_f<IT>(v.x); X[i + 1] = from_f<IT>(v.y);
+      X[i + 2] = from_f<IT>(v.z); X[i + 3] = from_f<IT>(v.w);
+    }
+  }
+}
+
+// W' = W*(1 - lr*wd) - lr*scale*O in the stored layout; O is read from the
+// working layout (transposed when tr).  Optionally O is written out too.
+template <typename PT>
+__global__ void __launch_bounds__(kNT) epilogue_kernel(
+    const __grid_constant__ SlicePtrs ptrs, int64_t M, int64_t N, int64_t n_pad, int tr,
+    float decay, float lr_scale, char* ws, size_t slice_ws, size_t off_O) {
+  const int s = blockIdx.y;
+  const float* O = reinterpret_cast<const float*>(ws + (size_t)s * slice_ws + off_O);
+  PT* W = static_cast<PT*>(ptrs.W[s]);
+  float* Oout = ptrs.O[s];
+  __shared__ float tile[32][33];
+  const int tiles_c = (int)((N + 31) / 32);
+  const int64_t r0 = (int64_t)(blockIdx.x / tiles_c) * 32;
+  const int64_t c0 = (int64_t)(blockIdx.x % tiles_c) * 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (tr) {
+    // stored (r, c) = working (c, r): stage working rows c0.. as a tile
+    for (int j = warp; j < 32; j += kNT / 32) {
+      const int64_t wr = c0 + j, wc = r0 + lane;  // working row, col
+      tile[j][lane] = O[wr * n_pad + wc];         // padded: always in range
+    }
+    __syncthreads();
+  }
+  for (int j = warp; j < 32; j += kNT / 32) {
+    const int64_t r = r0 + j, c = c0 + lane;
+    if (r < M && c < N) {
+      const float o = tr ? tile[lane][j] : O[r * n_pad + c];
+      const int64_t idx = r * N + c;
+      const float w = to_f(W[idx]);
+      W[idx] = from_f<PT>(fmaf(w, decay, -lr_scale * o));
+      if (Oout) Oout[idx] = o;
+    }
+  }
+}
+
+struct Offsets {
+  size_t V, X0, X1, A, B, part, inv;
+};
+
+Offsets dense_offsets(const Group& g, int mode) {
+  auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t mp = (size_t)g.m_pad, np = (size_t)g.n_pad;
+  const size_t e = mode == MUON_MODE_FP32 ? 4 : 2;
+  Offsets o;
+  size_t p = 0;
+  o.V = p;  p += a256(4 * mp * np);
+  o.X0 = p; p += a256(e * mp * np);
+  o.X1 = p; p += a256(e * mp * np);
+  o.A = p;  p += a256(e * mp * mp);
+  o.B = p;  p += a256(e * mp * mp);
+  o.part = p; p += a256(4 * (mp / kFrontTileR) * (np / kFrontTileC));
+  o.inv = p; p += 256;
+  return o;
+}
+
+template <typename IT>
+cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
+                      const StepArgs& st, char* ws, cudaStream_t s) {
+  const Offsets off = dense_offsets(g, mode);
+  const size_t sws = g.slice_ws;
+  const int64_t mp = g.m_pad, np = g.n_pad;
+  const int nblk = (int)((mp / kFrontTileR) * (np / kFrontTileC));
+  dim3 fgrid(nblk, ns);
+  if (g.dtype == MUON_BF16)
+    front_kernel<__nv_bfloat16><<<fgrid, kNT, 0, s>>>(ptrs, g.m, g.n, mp, np, g.tr, st.beta,
+                                                      st.nesterov, ws, sws, off.V, off.part);
+  else
+    front_kernel<float><<<fgrid, kNT, 0, s>>>(ptrs, g.m, g.n, mp, np, g.tr, st.beta,
+                                              st.nesterov, ws, sws, off.V, off.part);
+  finalize_kernel<<<ns, kNT, 0, s>>>(ws, sws, off.part, off.inv, nblk, st.eps);
+  const int64_t cnt = mp * np;
+  int nb = (int)((cnt / 4 + kNT - 1) / kNT);
+  if (nb > 1184) nb = 1184;
+  normalize_kernel<IT><<<dim3(nb, ns), kNT, 0, s>>>(ws, sws, off.V, off.X0, off.inv, cnt,
+                                                     st.T == 0 ? 1 : 0);
+  size_t xin = off.X0, xout = off.X1;
+  for (int t = 0; t < st.T; ++t) {
+    const bool last = t == st.T - 1;
+    GemmBatch gb;
+    gb.batch = ns;
+    gb.stride_bytes = sws;
+    // A = X X^T                         [m_pad, m_pad], K = n_pad
+    gb.M = mp; gb.N = mp; gb.K = np;
+    gb.A = ws + xin; gb.B = ws + xin; gb.C = nullptr; gb.D = ws + off.A;
+    gb.alpha = 1.f; gb.beta = 0.f;
+    cudaError_t e = gemm_nt<IT, IT>(gb, s);
+    if (e != cudaSuccess) return e;
+    // B = c*(A A) + b*A                 A symmetric: A A = A A^T
+    gb.M = mp; gb.N = mp; gb.K = mp;
+    gb.A = ws + off.A; gb.B = ws + off.A; gb.C = ws + off.A; gb.D = ws + off.B;
+    gb.alpha = st.c; gb.beta = st.b;
+    e = gemm_nt<IT, IT>(gb, s);
+    if (e != cudaSuccess) return e;
+    // X' = B X + a*X                    [m_pad, n_pad], K = m_pad, X is N-major
+    gb.M = mp; gb.N = np; gb.K = mp;
+    gb.A = ws + off.B; gb.B = ws + xin; gb.C = ws + xin;
+    gb.alpha = 1.f; gb.beta = st.a;
+    if (last) {
+      gb.D = ws + off.V;
+      e = gemm_nn<IT, float>(gb, s);
+    } else {
+      gb.D = ws + xout;
+      e = gemm_nn<IT, IT>(gb, s);
+    }
+    if (e != cudaSuccess) return e;
+    const size_t tmp = xin; xin = xout; xout = tmp;
+  }
+  const int tiles = (int)(((g.M + 31) / 32) * ((g.N + 31) / 32));
+  const float decay = 1.f - st.lr * st.wd;
+  const float lrs = st.lr * g.scale;
+  if (g.dtype == MUON_BF16)
+    epilogue_kernel<__nv_bfloat16><<<dim3(tiles, ns), kNT, 0, s>>>(ptrs, g.M, g.N, np, g.tr,
+                                                                  decay, lrs, ws, sws, off.V);
+  else
+    epilogue_kernel<float><<<dim3(tiles, ns), kNT, 0, s>>>(ptrs, g.M, g.N, np, g.tr, decay,
+                                                          lrs, ws, sws, off.V);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int dense_launches(int ns_steps) { return 4 + 3 * ns_steps; }
+
+cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& ptrs,
+                                     int nslices, const StepArgs& st, char* ws,
+                                     int* /*err_word*/, cudaStream_t s) {
+  if (mode == MUON_MODE_FP32) return run_dense<float>(g, mode, ptrs, nslices, st, ws, s);
+  return run_dense<__half>(g, mode, ptrs, nslices, st, ws, s);
+}
+
+}  // namespace muon

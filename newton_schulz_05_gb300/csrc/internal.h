@@ -1,0 +1,85 @@
+// Internal declarations shared by the host planner, the step driver and the
+// kernel launchers of libmuon.  Not part of the public C ABI (include/muon.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "muon.h"
+
+namespace muon {
+
+constexpr size_t kHeaderBytes = 256;   // workspace header: device error word
+constexpr int kMaxSlicesPerLaunch = 512;
+constexpr int kDensePad = 128;         // dense working dims are padded to this
+constexpr int kFrontTileR = 32;        // front kernel tile (working layout)
+constexpr int kFrontTileC = 128;
+
+// device error codes written into the workspace header
+constexpr int kDevErrTimeout = 1;
+
+struct Group {
+  int64_t M = 0, N = 0, m = 0, n = 0;
+  int dtype = 0;
+  int tr = 0;
+  float scale = 1.f;
+  int kernel = MUON_KERNEL_DENSE;
+  std::vector<int> slice_param;  // parameter of each slice, group order
+  std::vector<int64_t> slice_e;  // slice index inside that parameter
+  int count() const { return (int)slice_param.size(); }
+  // skinny kernel configuration
+  int mb = 0;        // row blocks of 8 (padded m / 8)
+  int nw = 0;        // warps per CTA
+  int cluster = 0;   // CTAs per slice
+  int sc_per_cta = 0, sc_per_warp = 0;  // 32-column superchunks
+  // dense path
+  int64_t m_pad = 0, n_pad = 0;
+  int chunk = 0;           // slices per chunk
+  size_t slice_ws = 0;     // workspace bytes per slice
+};
+
+}  // namespace muon
+
+struct muon_plan_s {
+  std::vector<muon_shape> shapes;
+  std::vector<int> param_first_slice;   // global slice id of (p, 0)
+  std::vector<int> slice_group, slice_index;
+  std::vector<muon::Group> groups;
+  muon_options opt;
+  size_t ws_bytes = 0;
+};
+
+namespace muon {
+
+// Per-slice pointers of one launch (passed by value as a kernel parameter).
+struct SlicePtrs {
+  void* W[kMaxSlicesPerLaunch];
+  const void* G[kMaxSlicesPerLaunch];
+  float* Mom[kMaxSlicesPerLaunch];
+  float* O[kMaxSlicesPerLaunch];     // null entries: O not requested
+};
+
+struct StepArgs {
+  float lr, beta, wd;
+  int nesterov;
+  int T;
+  float a, b, c;
+  float eps;
+};
+
+size_t dense_slice_ws(const Group& g, int mode);
+
+// launchers; each returns cudaSuccess or the launch error
+cudaError_t launch_skinny(const Group& g, const SlicePtrs& ptrs, int nslices,
+                          const StepArgs& st, int* err_word, cudaStream_t s);
+
+cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& ptrs,
+                                     int nslices, const StepArgs& st, char* ws,
+                                     int* err_word, cudaStream_t s);
+
+int dense_launches(int ns_steps);
+
+}  // namespace muon

@@ -1,0 +1,104 @@
+// muon_step: validates its arguments, then enqueues, group by group, the
+// launches of one Muon step on the caller's stream.  No allocation, no host
+// synchronisation.  Skinny groups run the fused on-chip kernel (one launch
+// per <= 512 slices); dense groups run the front / GEMM / epilogue sequence
+// per chunk of slices that fits the workspace.
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+
+using namespace muon;
+
+namespace {
+
+muon_status step_impl(const muon_plan_t* P, void* const* params, const void* const* grads,
+                      float* const* momentum, float lr, float beta, float wd, int nesterov,
+                      int ns_steps, const float* coeffs, void* workspace, size_t ws_bytes,
+                      void* stream, float* const* ortho) {
+  if (!P) return MUON_ERR_INVALID_ARG;
+  const int np = (int)P->shapes.size();
+  if (np > 0 && (!params || !grads || !momentum)) return MUON_ERR_INVALID_ARG;
+  for (int p = 0; p < np; ++p)
+    if (!params[p] || !grads[p] || !momentum[p] || (ortho && !ortho[p])) return MUON_ERR_INVALID_ARG;
+  if (ns_steps < 0 || ns_steps > 1000) return MUON_ERR_INVALID_ARG;
+  if (!std::isfinite(lr) || !std::isfinite(beta) || !std::isfinite(wd)) return MUON_ERR_INVALID_ARG;
+  if (!workspace) return MUON_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return MUON_ERR_ALIGNMENT;
+  if (ws_bytes < P->ws_bytes) return MUON_ERR_WORKSPACE;
+  StepArgs st;
+  st.lr = lr; st.beta = beta; st.wd = wd; st.nesterov = nesterov ? 1 : 0;
+  st.T = ns_steps;
+  st.a = coeffs ? coeffs[0] : 3.4445f;
+  st.b = coeffs ? coeffs[1] : -4.7750f;
+  st.c = coeffs ? coeffs[2] : 2.0315f;
+  if (!std::isfinite(st.a) || !std::isfinite(st.b) || !std::isfinite(st.c)) return MUON_ERR_INVALID_ARG;
+  st.eps = P->opt.eps;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* err_word = reinterpret_cast<int*>(ws);
+  char* body = ws + kHeaderBytes;
+
+  SlicePtrs ptrs;
+  for (const Group& g : P->groups) {
+    const int cnt = g.count();
+    const size_t es = g.dtype == MUON_BF16 ? 2 : 4;
+    const int64_t mn = g.M * g.N;
+    const int per = g.kernel == MUON_KERNEL_SKINNY ? kMaxSlicesPerLaunch : g.chunk;
+    for (int c0 = 0; c0 < cnt; c0 += per) {
+      const int ns = cnt - c0 < per ? cnt - c0 : per;
+      for (int i = 0; i < ns; ++i) {
+        const int p = g.slice_param[c0 + i];
+        const int64_t off = g.slice_e[c0 + i] * mn;
+        ptrs.W[i] = static_cast<char*>(params[p]) + off * es;
+        ptrs.G[i] = static_cast<const char*>(grads[p]) + off * es;
+        ptrs.Mom[i] = momentum[p] + off;
+        ptrs.O[i] = ortho ? ortho[p] + off : nullptr;
+      }
+      cudaError_t e;
+      if (g.kernel == MUON_KERNEL_SKINNY)
+        e = launch_skinny(g, ptrs, ns, st, err_word, s);
+      else
+        e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body, err_word, s);
+      if (e != cudaSuccess) return MUON_ERR_CUDA;
+    }
+  }
+  return MUON_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+muon_status muon_step(const muon_plan_t* P, void* const* params, const void* const* grads,
+                      float* const* momentum, float lr, float beta, float wd, int nesterov,
+                      int ns_steps, const float* coeffs, void* workspace, size_t ws_bytes,
+                      void* stream) {
+  return step_impl(P, params, grads, momentum, lr, beta, wd, nesterov, ns_steps, coeffs,
+                   workspace, ws_bytes, stream, nullptr);
+}
+
+muon_status muon_step_ortho(const muon_plan_t* P, void* const* params,
+                            const void* const* grads, float* const* momentum, float lr,
+                            float beta, float wd, int nesterov, int ns_steps,
+                            const float* coeffs, void* workspace, size_t ws_bytes,
+                            void* stream, float* const* ortho) {
+  if (!ortho) return MUON_ERR_INVALID_ARG;
+  return step_impl(P, params, grads, momentum, lr, beta, wd, nesterov, ns_steps, coeffs,
+                   workspace, ws_bytes, stream, ortho);
+}
+
+muon_status muon_workspace_error(const void* workspace, void* stream, int clear, int* code) {
+  if (!workspace || !code) return MUON_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int h = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MUON_ERR_CUDA;
+  if (cudaMemcpy(&h, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MUON_ERR_CUDA;
+  if (clear && cudaMemset(const_cast<void*>(workspace), 0, sizeof(int)) != cudaSuccess)
+    return MUON_ERR_CUDA;
+  *code = h == 0 ? MUON_OK : MUON_ERR_DEVICE_TIMEOUT;
+  return MUON_OK;
+}
+
+}  // extern "C"

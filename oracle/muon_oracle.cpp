@@ -141,7 +141,7 @@ void oracle_newton_schulz(int64_t M, int64_t N, const double* X_in, int T,
   for (int64_t i = 0; i < m; ++i)
     for (int64_t k = 0; k < n; ++k)
       X[i * n + k] = tr ? X_in[k * N + i] : X_in[i * n + k];
-  std::vector<double> A((size_t)(m * m)), B((size_t)(m * m));
+  std::vector<double> A((size_t)(m * m)), At((size_t)(m * m)), B((size_t)(m * m));
   for (int t = 0; t < T; ++t) {
     // A = X X^T
     parallel_rows(m, threads, [&](int64_t r0, int64_t r1) {
@@ -152,12 +152,15 @@ void oracle_newton_schulz(int64_t M, int64_t N, const double* X_in, int T,
           A[i * m + j] = acc;
         }
     });
-    // B = b*A + c*(A A)
+    // B = b*A + c*(A A); the second factor is read from a transposed copy
+    // At[j][k] = A[k][j] so that both operands stream along rows
+    for (int64_t i = 0; i < m; ++i)
+      for (int64_t j = 0; j < m; ++j) At[j * m + i] = A[i * m + j];
     parallel_rows(m, threads, [&](int64_t r0, int64_t r1) {
       for (int64_t i = r0; i < r1; ++i)
         for (int64_t j = 0; j < m; ++j) {
           double acc = 0.0;
-          for (int64_t k = 0; k < m; ++k) acc += A[i * m + k] * A[k * m + j];
+          for (int64_t k = 0; k < m; ++k) acc += A[i * m + k] * At[j * m + k];
           B[i * m + j] = b * A[i * m + j] + c * acc;
         }
     });

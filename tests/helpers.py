@@ -1,0 +1,142 @@
+"""Shared helpers of the GPU parity tests: run libmuon on seeded inputs and
+compare with the fp64 oracle on the same host bytes.
+
+Tolerances (fixed for the Muon step):
+  * O, per slice: relative Frobenius error <= 2e-2 in the fp16 tensor-core
+    mode and <= 1e-4 in the fp32 mode;
+  * momentum: |M'_gpu - M'_oracle| <= 1e-6 * (beta |M| + |G|) elementwise
+    (one fp32 multiply-add of fp64-exact inputs);
+  * bf16 parameters: within one bf16 ulp of the round-to-nearest-even value
+    of the oracle's W'; fp32 parameters: relative Frobenius error of
+    W' - W within the O tolerance.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+TOL = {"tc16": 2e-2, "fp32": 1e-4}
+HOST_THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def muon():
+    from newton_schulz_05_gb300 import build
+    build.build()
+    import newton_schulz_05_gb300 as m
+    m.load()
+    return m
+
+
+def slices(t):
+    return [t] if t.dim() == 2 else [t[e] for e in range(t.shape[0])]
+
+
+def make_inputs(shapes, dtype, grad_std=1e-2, seed=0, steps=1, device="cpu", param_std=0.02):
+    W = [synth.draw(s, param_std, synth.param_seed(1, i), dtype, device) for i, s in enumerate(shapes)]
+    Gs = [[synth.draw(s, grad_std, synth.param_seed(seed + t, i), dtype, device)
+           for i, s in enumerate(shapes)] for t in range(steps)]
+    M = [torch.zeros(s, dtype=torch.float32, device=device) for s in shapes]
+    return W, Gs, M
+
+
+def gpu_step(plan, W, G, M, hp, ortho=True, ws=None):
+    """One step on the GPU.  W, G, M: lists of CUDA tensors (updated in place
+    for W and M).  Returns the list of O tensors (or None)."""
+    m = muon()
+    if ws is None:
+        ws = m.alloc_workspace(plan)
+    O = [torch.empty(w.shape, dtype=torch.float32, device=w.device) for w in W] if ortho else None
+    m.step(plan, W, G, M, lr=hp["lr"], beta=hp["beta"], wd=hp["wd"], nesterov=hp["nesterov"],
+           ns_steps=hp["ns_steps"], coeffs=hp.get("coeffs", synth.Workload("", (), torch.float32, 1).coeffs),
+           workspace=ws, ortho=O)
+    torch.cuda.synchronize()
+    assert m.workspace_error(ws) == 0
+    return O
+
+
+def oracle_step(W, G, M, hp, which=None):
+    """fp64 oracle over the slices of W/G/M (CPU tensors).  `which` selects
+    (param, slice) pairs; default all.  Returns {(p, e): (W', M', O)}."""
+    keys, ws, gs, ms = [], [], [], []
+    for p in range(len(W)):
+        sw, sg, sm = slices(W[p]), slices(G[p]), slices(M[p])
+        for e in range(len(sw)):
+            if which is not None and (p, e) not in which:
+                continue
+            keys.append((p, e)); ws.append(sw[e]); gs.append(sg[e]); ms.append(sm[e])
+    threads = HOST_THREADS
+    if len(keys) < threads or max(w.numel() for w in ws) > (1 << 20):
+        # few or big slices: one at a time, each spread over the host threads
+        out = {}
+        for k, w, g, mm in zip(keys, ws, gs, ms):
+            out[k] = oracle.muon_slice(w, g, mm, hp["lr"], hp["beta"], hp["wd"], hp["nesterov"],
+                                       T=hp["ns_steps"],
+                                       coeffs=hp.get("coeffs", oracle.DEFAULT_COEFFS),
+                                       threads=threads)
+        return out
+    wo, mo, oo, _ = oracle.muon_slices(ws, gs, ms, hp["lr"], hp["beta"], hp["wd"], hp["nesterov"],
+                                       T=hp["ns_steps"], coeffs=hp.get("coeffs", oracle.DEFAULT_COEFFS),
+                                       threads=threads)
+    return {k: (wo[i], mo[i], oo[i]) for i, k in enumerate(keys)}
+
+
+def rel_fro(a, b):
+    a = np.asarray(a, np.float64); b = np.asarray(b, np.float64)
+    nb = np.sqrt((b * b).sum())
+    d = np.sqrt(((a - b) ** 2).sum())
+    if nb == 0:
+        return 0.0 if d == 0 else float("inf")
+    return d / nb
+
+
+def bf16_ulp(x):
+    x = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.where(x > 0, x, 1.0)))
+    return np.where(x > 0, 2.0 ** (e - 7), 2.0 ** -133)
+
+
+def compare(key, gpu, ref, W0, G, M0, hp, mode, dtype, report=None):
+    """Assert one slice's GPU results against the oracle's."""
+    Wg, Mg, Og = [np.asarray(x.double().cpu().numpy(), np.float64) for x in gpu]
+    Wr, Mr, Or = ref
+    W0 = np.asarray(W0.double().cpu().numpy()); G = np.asarray(G.double().cpu().numpy())
+    M0 = np.asarray(M0.double().cpu().numpy())
+    tol = TOL[mode]
+    if Og is not None:
+        e = rel_fro(Og, Or)
+        if report is not None:
+            report.append((key, e))
+        assert e <= tol, "slice %s: O relative error %.3g > %.1g" % (key, e, tol)
+    bound = 1e-6 * (hp["beta"] * np.abs(M0) + np.abs(G)) + 1e-30
+    assert np.all(np.abs(Mg - Mr) <= bound), "slice %s: momentum mismatch" % (key,)
+    if dtype == torch.bfloat16:
+        Wr_b = torch.from_numpy(Wr).to(torch.bfloat16).double().numpy()
+        ulp = np.maximum(bf16_ulp(Wr_b), bf16_ulp(Wg))
+        bad = np.abs(Wg - Wr_b) > ulp
+        assert not bad.any(), "slice %s: %d params beyond one bf16 ulp" % (key, int(bad.sum()))
+    else:
+        e = rel_fro(Wg - W0, Wr - W0)
+        assert e <= tol, "slice %s: W'-W relative error %.3g" % (key, e)
+
+
+def run_and_check(shapes, dtype, hp, mode="tc16", grad_std=1e-2, seed=0, which=None,
+                  skinny_max_m=64, report=None):
+    """Seeded inputs -> GPU step (with O) and oracle -> compare every (or the
+    selected) slice.  Returns the plan."""
+    m = muon()
+    W, Gs, M = make_inputs(shapes, dtype, grad_std=grad_std, seed=seed)
+    G = Gs[0]
+    plan = m.Plan([(tuple(s), dtype) for s in shapes], mode=mode, skinny_max_m=skinny_max_m)
+    Wd = [w.cuda() for w in W]; Gd = [g.cuda() for g in G]; Md = [x.cuda() for x in M]
+    O = gpu_step(plan, Wd, Gd, Md, hp)
+    ref = oracle_step(W, G, M, hp, which)
+    for (p, e), r in ref.items():
+        gp = (slices(Wd[p])[e], slices(Md[p])[e], slices(O[p])[e])
+        compare((p, e), gp, r, slices(W[p])[e], slices(G[p])[e], slices(M[p])[e], hp, mode, dtype,
+                report)
+    return plan

@@ -1,0 +1,162 @@
+"""The C-ABI boundary on the CPU: the library loads, exports every symbol the
+header declares, and its host-only planner equals the oracle's plan bit for
+bit (group ids, indices, dims, transposition flag, float bits of the scale).
+No compute call is made here; muon_plan touches no device."""
+import ctypes
+import os
+import re
+import struct
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def muon():
+    from newton_schulz_05_gb300 import build
+    build.build()
+    import newton_schulz_05_gb300 as m
+    m.load()
+    return m
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "muon.h")).read()
+    return sorted(set(re.findall(r"MUON_API\s+[\w\s\*]+?\b(muon_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    fns = header_functions()
+    for f in ["muon_plan", "muon_step", "muon_plan_destroy", "muon_status_string"]:
+        assert f in fns
+
+
+def test_library_exports_every_declared_symbol(muon):
+    L = muon.load()
+    for f in header_functions():
+        assert hasattr(L, f), f
+    assert sorted(header_functions()) == sorted(muon.EXPORTS)
+
+
+def _oracle_dt(d):
+    return "bf16" if d == 0 else "f32"
+
+
+def _compare_plan(muon, shapes, dtypes_t, **kw):
+    import torch
+    plan = muon.Plan([(s, d) for s, d in zip(shapes, dtypes_t)], **kw)
+    dts = ["bf16" if d == torch.bfloat16 else "f32" for d in dtypes_t]
+    sg, si, groups = oracle.plan(shapes, dts)
+    got = plan.groups()
+    assert len(got) == len(groups)
+    for a, b in zip(got, groups):
+        assert (a["M"], a["N"], a["count"], bool(a["tr"])) == (b["M"], b["N"], b["count"], b["tr"])
+        assert _oracle_dt(a["dtype"]) == b["dtype"]
+        assert struct.pack("<f", a["scale"]) == struct.pack("<f", b["scale"])
+        assert (a["m"], a["n"]) == (min(a["M"], a["N"]), max(a["M"], a["N"]))
+    s = 0
+    for p, shp in enumerate(shapes):
+        E = shp[0] if len(shp) == 3 else 1
+        for e in range(E):
+            assert plan.slice(p, e) == (sg[s], si[s])
+            s += 1
+    assert plan.num_slices == s
+    return plan
+
+
+def test_plan_matches_oracle_random(muon):
+    import torch
+    rng = np.random.default_rng(21)
+    dims = [1, 7, 24, 64, 65, 130, 1408]
+    for _ in range(40):
+        shapes, dts = [], []
+        for _ in range(rng.integers(1, 10)):
+            if rng.random() < 0.4:
+                shapes.append((int(rng.integers(1, 4)), int(rng.choice(dims)), int(rng.choice(dims))))
+            else:
+                shapes.append((int(rng.choice(dims)), int(rng.choice(dims))))
+            dts.append(torch.bfloat16 if rng.random() < 0.7 else torch.float32)
+        _compare_plan(muon, shapes, dts)
+        _compare_plan(muon, shapes, dts, mode="fp32")
+
+
+@pytest.mark.parametrize("name", ["fp32_24x1024", "skinny_74x24x10240", "stacks_experts",
+                                  "dense_24L", "moe_24L"])
+def test_plan_matches_oracle_on_workloads(muon, name):
+    import synth
+    w = synth.workload(name)
+    plan = _compare_plan(muon, list(w.shapes), [w.dtype] * len(w.shapes))
+    kinds = {(g["m"], g["n"]): g["kernel"] for g in plan.groups()}
+    # the [24, 10240] batches run fused on chip, the rest on the dense path
+    for (m, n), k in kinds.items():
+        assert k == (muon.KERNEL_SKINNY if m <= 64 else muon.KERNEL_DENSE)
+
+
+def test_plan_skinny_cluster_configuration(muon):
+    import torch
+    plan = muon.Plan([((24, 10240), torch.bfloat16)] * 74)
+    (g,) = plan.groups()
+    assert g["kernel"] == muon.KERNEL_SKINNY and g["cluster"] == 2 and g["count"] == 74
+    assert plan.launches(5) == 1
+    assert plan.workspace_bytes == 256
+
+
+def test_plan_rejects_bad_input(muon):
+    import torch
+    with pytest.raises(muon.MuonError) as e:
+        muon.Plan([((5,), torch.bfloat16)])
+    assert e.value.status == -2
+    with pytest.raises(muon.MuonError) as e:
+        muon.Plan([((0, 4), torch.bfloat16)])
+    assert e.value.status == -2
+    with pytest.raises(muon.MuonError) as e:
+        muon.Plan([((3, 4), 7)])
+    assert e.value.status == -3
+    L = muon.load()
+    assert L.muon_plan(None, 1, None, None) == -1
+    assert muon.status_string(-7) == "workspace too small for the plan"
+
+
+def test_step_rejects_bad_arguments_before_any_launch(muon):
+    # argument checks run on the host and return before touching a device
+    import torch
+    plan = muon.Plan([((24, 64), torch.bfloat16)])
+    L = muon.load()
+    P = ctypes.c_void_p * 1
+    fake = P(ctypes.c_void_p(0x1000))
+    c = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    # null workspace
+    assert L.muon_step(plan.handle, fake, fake, fake, 0.02, 0.95, 0.1, 1, 5, c, None, 256, None) == -1
+    # misaligned workspace
+    assert L.muon_step(plan.handle, fake, fake, fake, 0.02, 0.95, 0.1, 1, 5, c,
+                       ctypes.c_void_p(0x1008), 4096, None) == -4
+    # workspace too small
+    assert L.muon_step(plan.handle, fake, fake, fake, 0.02, 0.95, 0.1, 1, 5, c,
+                       ctypes.c_void_p(0x1000), 16, None) == -7
+    # negative step count, null parameter pointer, non-finite lr
+    assert L.muon_step(plan.handle, fake, fake, fake, 0.02, 0.95, 0.1, 1, -1, c,
+                       ctypes.c_void_p(0x1000), 4096, None) == -1
+    nul = P(ctypes.c_void_p(0))
+    assert L.muon_step(plan.handle, nul, fake, fake, 0.02, 0.95, 0.1, 1, 5, c,
+                       ctypes.c_void_p(0x1000), 4096, None) == -1
+    assert L.muon_step(plan.handle, fake, fake, fake, float("nan"), 0.95, 0.1, 1, 5, c,
+                       ctypes.c_void_p(0x1000), 4096, None) == -1
+    assert L.muon_step_ortho(plan.handle, fake, fake, fake, 0.02, 0.95, 0.1, 1, 5, c,
+                             ctypes.c_void_p(0x1000), 4096, None, None) == -1
+
+
+def test_workspace_cap_chunks_dense_groups(muon):
+    import torch
+    shapes = [((4, 300, 200), torch.bfloat16)]
+    full = muon.Plan(shapes)
+    (g,) = full.groups()
+    assert g["kernel"] == muon.KERNEL_DENSE and g["chunk"] == 4
+    per = (full.workspace_bytes - 256) // 4
+    capped = muon.Plan(shapes, workspace_cap=256 + 2 * per)
+    assert capped.groups()[0]["chunk"] == 2
+    assert capped.workspace_bytes == 256 + 2 * per
+    assert capped.launches(5) == 2 * full.launches(5)

@@ -20,8 +20,9 @@ MUTANTS = {
                                 "acc += X[i * n + k] * X[i * n + k];"),
     "poly_drops_c_term": ("B[i * m + j] = b * A[i * m + j] + c * acc;",
                           "B[i * m + j] = b * A[i * m + j] + c * A[i * m + j];"),
-    "poly_square_index": ("acc += A[i * m + k] * A[k * m + j];",
-                          "acc += A[i * m + k] * A[j * m + k] * 0.5 + A[i * m + k] * A[k * m + j] * 0.5 + 1e-9;"),
+    "poly_square_index": ("acc += A[i * m + k] * At[j * m + k];",
+                          "acc += A[i * m + k] * At[k * m + j] + 1e-9;"),
+    "poly_transpose_copy": ("At[j * m + i] = A[i * m + j];", "At[i * m + j] = A[i * m + j] * 1.0000001;"),
     "update_wrong_sign": ("Xn[i * n + k] = a * X[i * n + k] + row[k];",
                           "Xn[i * n + k] = a * X[i * n + k] - row[k];"),
     "update_drops_aX": ("Xn[i * n + k] = a * X[i * n + k] + row[k];",

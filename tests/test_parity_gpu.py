@@ -1,0 +1,187 @@
+"""GPU parity: libmuon (through the C ABI) against the fp64 oracle, element
+by element on seeded inputs, plus exact properties of the step.
+
+Sizes span several tiles and ragged tails on both kernel families: the fused
+on-chip kernel (min(M,N) <= 64) and the dense path; both 2D and 3D stacks,
+M < N and M > N (transposed), both parameter dtypes and both arithmetic
+modes.  Workload-size cases live in test_workloads_gpu.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import (TOL, compare, gpu_step, make_inputs, muon, oracle_step, rel_fro,
+                     run_and_check, slices)
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=0.02, beta=0.95, wd=0.1, nesterov=True, ns_steps=5, coeffs=oracle.DEFAULT_COEFFS)
+
+
+def test_fp32_single_matrix_24x1024_both_modes():
+    # one fp32 [24, 1024] parameter, grad ~ N(0, 1) seed 0, beta 0.95 Nesterov,
+    # 5 steps, lr 0.02, wd 0.1, a single step from zero momentum
+    for mode in ("tc16", "fp32"):
+        run_and_check([(24, 1024)], torch.float32, HP, mode=mode, grad_std=1.0)
+
+
+SKINNY = [(24, 1024), (24, 10240), (5, 77), (64, 300), (20, 33), (1, 1), (1, 500), (500, 1),
+          (8, 8), (40, 2000), (56, 130), (1000, 24), (300, 64), (17, 4099), (3, 24, 500)]
+
+
+@pytest.mark.parametrize("shape", SKINNY, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_skinny_kernel_matches_oracle(shape, dtype):
+    plan = run_and_check([shape], dtype, HP)
+    assert plan.groups()[0]["kernel"] == muon().KERNEL_SKINNY
+
+
+DENSE = [(130, 260), (256, 384), (300, 200), (65, 1000), (2, 200, 150), (128, 128), (129, 129),
+         (1000, 70)]
+
+
+@pytest.mark.parametrize("shape", DENSE, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mode", ["tc16", "fp32"])
+def test_dense_path_matches_oracle(shape, mode):
+    plan = run_and_check([shape], torch.bfloat16, HP, mode=mode)
+    assert plan.groups()[0]["kernel"] == muon().KERNEL_DENSE
+
+
+@pytest.mark.parametrize("shape", [(24, 1024), (3, 40, 300), (500, 24)], ids=str)
+def test_fp32_mode_on_skinny_shapes(shape):
+    plan = run_and_check([shape], torch.float32, HP, mode="fp32")
+    assert plan.groups()[0]["kernel"] == muon().KERNEL_DENSE
+
+
+def test_mixed_groups_one_call():
+    shapes = [(24, 700), (2, 24, 700), (200, 150), (150, 200), (700, 24), (24, 700)]
+    plan = run_and_check(shapes, torch.bfloat16, HP)
+    kinds = [g["kernel"] for g in plan.groups()]
+    assert len(kinds) == 4 and plan.groups()[0]["count"] == 4
+
+
+@pytest.mark.parametrize("shape", [(24, 1000), (200, 300)], ids=str)
+@pytest.mark.parametrize("T", [0, 1, 3])
+def test_ns_step_counts(shape, T):
+    run_and_check([shape], torch.bfloat16, dict(HP, ns_steps=T))
+
+
+@pytest.mark.parametrize("shape", [(24, 1000), (200, 300)], ids=str)
+def test_plain_momentum_and_cubic_coefficients(shape):
+    run_and_check([shape], torch.bfloat16, dict(HP, nesterov=False))
+    run_and_check([shape], torch.float32, dict(HP, coeffs=(1.5, -0.5, 0.0), ns_steps=10))
+
+
+@pytest.mark.parametrize("shape", [(24, 1000), (200, 300), (300, 200)], ids=str)
+def test_zero_gradient_is_pure_decay(shape):
+    m = muon()
+    W, Gs, M = make_inputs([shape], torch.bfloat16)
+    Wd = [W[0].cuda()]; Gd = [torch.zeros_like(Gs[0][0]).cuda()]; Md = [M[0].cuda()]
+    plan = m.Plan([(shape, torch.bfloat16)])
+    O = gpu_step(plan, Wd, Gd, Md, HP)
+    assert torch.count_nonzero(O[0]).item() == 0 and torch.count_nonzero(Md[0]).item() == 0
+    expect = (W[0].float() * np.float32(1 - 0.02 * 0.1)).to(torch.bfloat16)
+    assert torch.equal(Wd[0].cpu(), expect)
+
+
+@pytest.mark.parametrize("shape", [(24, 1000), (200, 300)], ids=str)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_zero_lr_and_wd_leave_params_unchanged(shape, dtype):
+    m = muon()
+    W, Gs, M = make_inputs([shape], dtype)
+    Wd = [W[0].cuda()]
+    plan = m.Plan([(shape, dtype)])
+    gpu_step(plan, Wd, [Gs[0][0].cuda()], [M[0].cuda()], dict(HP, lr=0.0, wd=0.0))
+    assert torch.equal(Wd[0].cpu(), W[0])
+
+
+@pytest.mark.parametrize("shapes", [[(24, 1000)] * 3, [(200, 300)] * 3], ids=["skinny", "dense"])
+def test_slice_results_do_not_depend_on_batch_mates(shapes):
+    # RFC section 2: slices are independent; a slice alone and inside a batch
+    # must give the same bits
+    m = muon()
+    W, Gs, M = make_inputs(shapes, torch.bfloat16)
+    full = m.Plan([(s, torch.bfloat16) for s in shapes])
+    Wd = [w.cuda() for w in W]; Md = [x.cuda() for x in M]
+    O = gpu_step(full, Wd, [g.cuda() for g in Gs[0]], Md, HP)
+    one = m.Plan([(shapes[1], torch.bfloat16)])
+    W1 = [W[1].cuda()]; M1 = [M[1].cuda()]
+    O1 = gpu_step(one, W1, [Gs[0][1].cuda()], M1, HP)
+    assert torch.equal(O1[0], O[1]) and torch.equal(W1[0], Wd[1]) and torch.equal(M1[0], Md[1])
+
+
+@pytest.mark.parametrize("shapes", [[(24, 10240)] * 4, [(2, 300, 200)]], ids=["skinny", "dense"])
+def test_bitwise_deterministic(shapes):
+    m = muon()
+    W, Gs, M = make_inputs(shapes, torch.bfloat16)
+    plan = m.Plan([(s, torch.bfloat16) for s in shapes])
+    outs = []
+    for _ in range(2):
+        Wd = [w.cuda() for w in W]; Md = [x.cuda() for x in M]
+        O = gpu_step(plan, Wd, [g.cuda() for g in Gs[0]], Md, HP)
+        outs.append((Wd, Md, O))
+    for a, b in zip(outs[0], outs[1]):
+        assert all(torch.equal(x, y) for x, y in zip(a, b))
+
+
+def test_checkpoint_resume_is_bitwise():
+    # the caller owns all state: 10 steps == 5 steps, copy out/in, 5 steps
+    m = muon()
+    shapes = [(24, 1000), (200, 300)]
+    W, Gs, M = make_inputs(shapes, torch.bfloat16, steps=10)
+    plan = m.Plan([(s, torch.bfloat16) for s in shapes])
+    Wa = [w.cuda() for w in W]; Ma = [x.cuda() for x in M]
+    for t in range(10):
+        gpu_step(plan, Wa, [g.cuda() for g in Gs[t]], Ma, HP, ortho=False)
+    Wb = [w.cuda() for w in W]; Mb = [x.cuda() for x in M]
+    for t in range(5):
+        gpu_step(plan, Wb, [g.cuda() for g in Gs[t]], Mb, HP, ortho=False)
+    Wc = [w.cpu().cuda() for w in Wb]; Mc = [x.cpu().cuda() for x in Mb]
+    del Wb, Mb
+    for t in range(5, 10):
+        gpu_step(plan, Wc, [g.cuda() for g in Gs[t]], Mc, HP, ortho=False)
+    assert all(torch.equal(a, b) for a, b in zip(Wa, Wc))
+    assert all(torch.equal(a, b) for a, b in zip(Ma, Mc))
+
+
+def test_chunked_workspace_gives_same_bits():
+    m = muon()
+    shapes = [(5, 200, 150)]
+    W, Gs, M = make_inputs(shapes, torch.bfloat16)
+    full = m.Plan([(shapes[0], torch.bfloat16)])
+    per = (full.workspace_bytes - 256) // 5
+    capped = m.Plan([(shapes[0], torch.bfloat16)], workspace_cap=256 + 2 * per)
+    assert capped.groups()[0]["chunk"] == 2
+    res = []
+    for plan in (full, capped):
+        Wd = [W[0].cuda()]; Md = [M[0].cuda()]
+        O = gpu_step(plan, Wd, [Gs[0][0].cuda()], Md, HP)
+        res.append((Wd[0], Md[0], O[0]))
+    assert all(torch.equal(a, b) for a, b in zip(*res))
+
+
+def test_skinny_and_dense_paths_agree():
+    # the same skinny group through the fused kernel and through the dense
+    # GEMM path: both within tolerance of the oracle and of each other
+    m = muon()
+    shape = (24, 2048)
+    W, Gs, M = make_inputs([shape], torch.bfloat16)
+    Os = []
+    for smax in (64, 0):
+        plan = m.Plan([(shape, torch.bfloat16)], skinny_max_m=smax)
+        O = gpu_step(plan, [W[0].cuda()], [Gs[0][0].cuda()], [M[0].cuda()], HP)
+        Os.append(O[0].cpu().double().numpy())
+    assert rel_fro(Os[0], Os[1]) < 2 * TOL["tc16"]
+
+
+def test_nan_gradient_propagates():
+    m = muon()
+    for shape in [(24, 512), (200, 300)]:
+        W, Gs, M = make_inputs([shape], torch.float32)
+        G = Gs[0][0].clone()
+        G[3, 7] = float("nan")
+        plan = m.Plan([(shape, torch.float32)])
+        Wd = [W[0].cuda()]
+        gpu_step(plan, Wd, [G.cuda()], [M[0].cuda()], HP, ortho=False)
+        assert torch.isnan(Wd[0]).any()
