@@ -1,0 +1,419 @@
+// Batched fp16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA)
+// for the dense Newton-Schulz products:
+//   A = X X^T          (symmetric output: upper tiles only, mirrored)
+//   B = c*A*A + b*A    (symmetric output, C = A)
+//   X' = B*X + a*X     (B operand N-major, C = X; fp32 output on the last step)
+// D[b] = alpha * A[b] op(B[b]) + beta * C[b], fp32 accumulation in TMEM.
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0    TMA producer: 128x64 A box and 256x64 B box per stage (or four
+//             64x64 N-major boxes), 4-stage ring, 128-byte swizzle;
+//   warp 1    allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//             one thread issues tcgen05.mma (M=128, N=256, K=16);
+//   warps 2-5 epilogue: tcgen05.ld of their 32 TMEM lanes, alpha/beta, store;
+//             the accumulator is double-buffered so the epilogue of tile t
+//             overlaps the MMAs of tile t+1.
+// Every mbarrier wait is bounded; when a budget runs out the kernel records
+// an error word, drains its own copies in flight and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_gemm.h"
+
+namespace muon {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int NTHREADS = 192;
+constexpr uint32_t kWaitLimit = 1u << 26;       // try_wait polls before giving up
+
+struct TcParams {
+  int M, N, K;
+  int tiles_m, tiles_n, tiles_per_batch, total_tiles;
+  size_t stride;       // bytes between batch entries (C and D)
+  const __half* C;     // [M, N] of batch 0, or null
+  void* D;             // [M, N] of batch 0
+  int d_f32;
+  float alpha, beta;
+  int sym;
+  int b_mn;
+  uint32_t idesc;
+  int* err;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// bounded wait for the phase of parity `parity` to complete
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5}], [%2];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// shared-memory matrix descriptor, 128-byte swizzle, sm_100 version bits
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;             // descriptor version
+  d |= (uint64_t)2 << 61;             // SWIZZLE_128B
+  return d;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+// tile index -> (batch, row tile I, col tile J); symmetric outputs only
+// enumerate tiles whose second 128-column half reaches the diagonal
+__device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& b, int& I, int& J) {
+  b = t / p.tiles_per_batch;
+  int r = t % p.tiles_per_batch;
+  if (!p.sym) {
+    I = r / p.tiles_n;
+    J = r % p.tiles_n;
+    return;
+  }
+  for (I = 0; I < p.tiles_m; ++I) {
+    const int cnt = p.tiles_n - I / 2;
+    if (r < cnt) { J = I / 2 + r; return; }
+    r -= cnt;
+  }
+  I = 0; J = 0;  // unreachable for valid t
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ TcParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
+                     smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int kblocks = p.K / BK;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicExch(p.err, kDevErrTimeout);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < p.total_tiles && !*abort_flag; t += gridDim.x) {
+        int b, I, J;
+        tile_coords(p, t, b, I, J);
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1)) { fail(); break; }
+          unsigned char* sa = smem + s * STAGE_BYTES;
+          unsigned char* sb = sa + A_BYTES;
+          mbar_expect_tx(&full[s], STAGE_BYTES);
+          tma_load_3d(sa, &tmA, &full[s], kb * BK, I * BM, b);
+          if (!p.b_mn) {
+            tma_load_3d(sb, &tmB, &full[s], kb * BK, J * BN, b);
+          } else {
+            #pragma unroll
+            for (int q = 0; q < BN / 64; ++q)
+              tma_load_3d(sb + q * (64 * BK * 2), &tmB, &full[s], J * BN + q * 64, kb * BK, b);
+          }
+        }
+      }
+      // drain: every issued load must land before the CTA may exit
+      const uint32_t last = it;
+      for (uint32_t k = (last > STAGES ? last - STAGES : 0); k < last; ++k)
+        if (!mbar_wait(&full[k % STAGES], (k / STAGES) & 1)) { fail(); break; }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, tl = 0;
+      for (int t = blockIdx.x; t < p.total_tiles && !*abort_flag; t += gridDim.x, ++tl) {
+        const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], aph ^ 1)) { fail(); break; }
+        tc_fence_after();
+        const uint32_t dt = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&full[s], ph)) { fail(); ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          #pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc(sa + k * 32, 16, 1024);
+            const uint64_t bd = p.b_mn ? sdesc(sb + k * 2048, 64 * BK * 2, 1024)
+                                       : sdesc(sb + k * 32, 16, 1024);
+            mma_f16(dt, ad, bd, p.idesc, (kb | k) != 0);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    // epilogue warps 2..5: TMEM lane quarter q = warp % 4
+    const int q = warp & 3;
+    uint32_t tl = 0;
+    for (int t = blockIdx.x; t < p.total_tiles && !*abort_flag; t += gridDim.x, ++tl) {
+      int b, I, J;
+      tile_coords(p, t, b, I, J);
+      const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], aph)) { fail(); break; }
+      tc_fence_after();
+      const int row = I * BM + q * 32 + lane;
+      const size_t boff = (size_t)b * p.stride;
+      const __half* Cb = p.C ? reinterpret_cast<const __half*>(reinterpret_cast<const char*>(p.C) + boff)
+                             : nullptr;
+      char* Db = reinterpret_cast<char*>(p.D) + boff;
+      #pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = J * BN + c * 32;
+        float v[32];
+        tm_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, v);
+        if (col0 >= p.N) continue;
+        const int cblk = col0 / 128;
+        if (p.sym && cblk < I) continue;  // lower block: written as a mirror by its owner
+        if (Cb && p.beta != 0.f) {
+          const uint4* cp = reinterpret_cast<const uint4*>(Cb + (size_t)row * p.N + col0);
+          #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 u = cp[j];
+            const __half2* h = reinterpret_cast<const __half2*>(&u);
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(h[e]);
+              v[8 * j + 2 * e] = fmaf(p.alpha, v[8 * j + 2 * e], p.beta * f.x);
+              v[8 * j + 2 * e + 1] = fmaf(p.alpha, v[8 * j + 2 * e + 1], p.beta * f.y);
+            }
+          }
+        } else {
+          #pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
+        }
+        if (p.d_f32) {
+          float4* dp = reinterpret_cast<float4*>(reinterpret_cast<float*>(Db) + (size_t)row * p.N + col0);
+          #pragma unroll
+          for (int j = 0; j < 8; ++j) dp[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+          __half* D = reinterpret_cast<__half*>(Db);
+          uint4* dp = reinterpret_cast<uint4*>(D + (size_t)row * p.N + col0);
+          #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 u;
+            __half2* h = reinterpret_cast<__half2*>(&u);
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
+            dp[j] = u;
+          }
+          if (p.sym && cblk > I) {
+            // mirror: D[col][row]; lanes hold consecutive rows -> coalesced
+            #pragma unroll
+            for (int j = 0; j < 32; ++j) D[(size_t)(col0 + j) * p.N + row] = __float2half_rn(v[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t batch,
+              uint64_t row_bytes, uint64_t batch_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {inner, outer, batch};
+  const cuuint64_t strides[2] = {row_bytes, batch_bytes};
+  const cuuint32_t box[3] = {box_inner, box_outer, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+uint32_t tc_idesc_f16(int m, int n, int b_mn) {
+  uint32_t d = 0;
+  d |= 1u << 4;                        // D format: f32
+  d |= 0u << 7;                        // A format: f16
+  d |= 0u << 10;                       // B format: f16
+  d |= (uint32_t)(b_mn ? 1 : 0) << 16; // B major: 0 = K, 1 = MN
+  d |= (uint32_t)(n >> 3) << 17;
+  d |= (uint32_t)(m >> 4) << 24;
+  return d;
+}
+
+size_t tc_gemm_smem_bytes() { return STAGES * STAGE_BYTES + 1024 + 256; }
+
+cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
+  if (g.M % BM || g.N % 128 || g.K % BK || g.batch < 1 || (g.sym && g.M != g.N))
+    return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, g.A, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.batch, (uint64_t)g.K * 2,
+                g.stride, BK, BM))
+    return cudaErrorInvalidValue;
+  const bool ok_b = g.b_mn
+      ? make_map(&tb, g.B, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)g.batch, (uint64_t)g.N * 2, g.stride,
+                 64, BK)
+      : make_map(&tb, g.B, (uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.batch, (uint64_t)g.K * 2, g.stride,
+                 BK, BN);
+  if (!ok_b) return cudaErrorInvalidValue;
+  TcParams p;
+  p.M = (int)g.M; p.N = (int)g.N; p.K = (int)g.K;
+  p.tiles_m = (int)(g.M / BM);
+  p.tiles_n = (int)((g.N + BN - 1) / BN);
+  if (g.sym) {
+    int cnt = 0;
+    for (int I = 0; I < p.tiles_m; ++I) cnt += p.tiles_n - I / 2;
+    p.tiles_per_batch = cnt;
+  } else {
+    p.tiles_per_batch = p.tiles_m * p.tiles_n;
+  }
+  p.total_tiles = p.tiles_per_batch * g.batch;
+  p.stride = g.stride;
+  p.C = static_cast<const __half*>(g.C);
+  p.D = g.D;
+  p.d_f32 = g.d_f32;
+  p.alpha = g.alpha; p.beta = g.beta;
+  p.sym = g.sym; p.b_mn = g.b_mn;
+  p.idesc = tc_idesc_f16(BM, BN, g.b_mn);
+  p.err = g.err;
+  const size_t smem = tc_gemm_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
+  tc_gemm_kernel<<<grid, NTHREADS, smem, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace muon
