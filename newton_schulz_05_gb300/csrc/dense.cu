@@ -21,6 +21,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "gemm.cuh"
+#include "tc_gemm.h"
 
 namespace muon {
 
@@ -190,7 +191,7 @@ Offsets dense_offsets(const Group& g, int mode) {
 
 template <typename IT>
 cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
-                      const StepArgs& st, char* ws, cudaStream_t s) {
+                      const StepArgs& st, char* ws, int* err_word, cudaStream_t s) {
   const Offsets off = dense_offsets(g, mode);
   const size_t sws = g.slice_ws;
   const int64_t mp = g.m_pad, np = g.n_pad;
@@ -209,6 +210,36 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   normalize_kernel<IT><<<dim3(nb, ns), kNT, 0, s>>>(ws, sws, off.V, off.X0, off.inv, cnt,
                                                      st.T == 0 ? 1 : 0);
   size_t xin = off.X0, xout = off.X1;
+  if constexpr (sizeof(IT) == 2) {
+    // fp16 operands: the three products on the tcgen05 tensor cores
+    for (int t = 0; t < st.T; ++t) {
+      const bool last = t == st.T - 1;
+      TcGemm g1;
+      g1.batch = ns; g1.stride = sws; g1.err = err_word;
+      // A = X X^T (symmetric)
+      g1.M = mp; g1.N = mp; g1.K = np;
+      g1.A = ws + xin; g1.B = ws + xin; g1.D = ws + off.A; g1.sym = 1;
+      cudaError_t e = tc_gemm(g1, s);
+      if (e != cudaSuccess) return e;
+      // B = c*A*A + b*A (symmetric; A A = A A^T)
+      TcGemm g2 = g1;
+      g2.K = mp;
+      g2.A = ws + off.A; g2.B = ws + off.A; g2.C = ws + off.A; g2.D = ws + off.B;
+      g2.alpha = st.c; g2.beta = st.b;
+      e = tc_gemm(g2, s);
+      if (e != cudaSuccess) return e;
+      // X' = B X + a*X, X as an N-major B operand; fp32 O on the last step
+      TcGemm g3;
+      g3.batch = ns; g3.stride = sws; g3.err = err_word;
+      g3.M = mp; g3.N = np; g3.K = mp;
+      g3.A = ws + off.B; g3.B = ws + xin; g3.C = ws + xin; g3.b_mn = 1;
+      g3.alpha = 1.f; g3.beta = st.a;
+      g3.D = ws + (last ? off.V : xout); g3.d_f32 = last ? 1 : 0;
+      e = tc_gemm(g3, s);
+      if (e != cudaSuccess) return e;
+      const size_t tmp = xin; xin = xout; xout = tmp;
+    }
+  } else
   for (int t = 0; t < st.T; ++t) {
     const bool last = t == st.T - 1;
     GemmBatch gb;
@@ -258,9 +289,9 @@ int dense_launches(int ns_steps) { return 4 + 3 * ns_steps; }
 
 cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& ptrs,
                                      int nslices, const StepArgs& st, char* ws,
-                                     int* /*err_word*/, cudaStream_t s) {
-  if (mode == MUON_MODE_FP32) return run_dense<float>(g, mode, ptrs, nslices, st, ws, s);
-  return run_dense<__half>(g, mode, ptrs, nslices, st, ws, s);
+                                     int* err_word, cudaStream_t s) {
+  if (mode == MUON_MODE_FP32) return run_dense<float>(g, mode, ptrs, nslices, st, ws, err_word, s);
+  return run_dense<__half>(g, mode, ptrs, nslices, st, ws, err_word, s);
 }
 
 }  // namespace muon
