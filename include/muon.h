@@ -162,6 +162,32 @@ MUON_API muon_status muon_step_ortho(const muon_plan_t* plan, void* const* param
 MUON_API muon_status muon_workspace_error(const void* workspace, void* stream, int clear,
                                  int* code);
 
+/*
+ * muon_step without a workspace argument, for callers that cannot allocate
+ * device memory: a host runtime that hands nearly all of the GPU's memory to
+ * its own pooled allocator at start-up, leaving none for a library's
+ * cudaMalloc, or a latency-bound caller that cannot afford a cudaMalloc,
+ * which may block and synchronise the device.  The RFC has no counterpart of
+ * this call.
+ *
+ * The scratch is one static device array of MUON_STATIC_WORKSPACE_BYTES,
+ * held by every GPU that loads the library until the process exits; no call
+ * allocates or frees anything.  Plans whose muon_plan_workspace_bytes exceed
+ * that size are rejected with MUON_ERR_WORKSPACE before any device work.
+ * The first call on each device, with that device current, looks up the
+ * array's device address and caches it; make that first call before any
+ * stream capture.  Every call shares the array and finds the previous call's
+ * contents there: the device error word is cleared at each call, everything
+ * else is written before it is read.  Calls whose work overlaps on the GPU
+ * (streams with no ordering between them) race on the array.  Arguments are
+ * those of muon_step.
+ */
+#define MUON_STATIC_WORKSPACE_BYTES (32u << 20)
+MUON_API muon_status muon_step_static(const muon_plan_t* plan, void* const* params,
+                                      const void* const* grads, float* const* momentum,
+                                      float lr, float beta, float wd, int nesterov,
+                                      int ns_steps, const float* coeffs, void* stream);
+
 /* Kernel launches muon_step makes for this plan and ns_steps (for
  * accounting; no device call). */
 MUON_API muon_status muon_plan_launches(const muon_plan_t* plan, int ns_steps, int* out);

@@ -57,7 +57,9 @@ class _GroupInfo(ctypes.Structure):
 EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
            "muon_plan_num_groups", "muon_plan_num_slices", "muon_plan_group",
            "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
-           "muon_plan_launches", "muon_plan_destroy", "muon_status_string"]
+           "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static"]
+
+STATIC_WORKSPACE_BYTES = 32 << 20   # MUON_STATIC_WORKSPACE_BYTES in include/muon.h
 
 _lib = None
 
@@ -86,6 +88,7 @@ def load(path: str = LIB_PATH):
                  ctypes.c_int, ctypes.POINTER(ctypes.c_float), vp, sz, vp]
     L.muon_step.argtypes = step_args
     L.muon_step_ortho.argtypes = step_args + [PP]
+    L.muon_step_static.argtypes = step_args[:10] + [vp]
     L.muon_workspace_error.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.muon_plan_launches.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.muon_plan_destroy.argtypes = [vp]
@@ -94,7 +97,8 @@ def load(path: str = LIB_PATH):
     L.muon_status_string.restype = ctypes.c_char_p
     for fn in ("muon_plan", "muon_plan_workspace_bytes", "muon_plan_num_groups",
                "muon_plan_num_slices", "muon_plan_group", "muon_plan_slice", "muon_step",
-               "muon_step_ortho", "muon_workspace_error", "muon_plan_launches"):
+               "muon_step_ortho", "muon_workspace_error", "muon_plan_launches",
+               "muon_step_static"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -233,6 +237,19 @@ def step(plan: Plan, params, grads, momentum, *, lr: float, beta: float, wd: flo
             if tuple(o.shape) != plan.shapes[i] or o.dtype != torch.float32 or not o.is_contiguous():
                 raise ValueError("ortho %d must be a contiguous fp32 tensor of the param's shape" % i)
         _check(L.muon_step_ortho(*args, _ptrs(ortho)), "muon_step_ortho")
+
+
+def step_static(plan: Plan, params, grads, momentum, *, lr: float, beta: float, wd: float,
+                nesterov: bool = True, ns_steps: int = 5, coeffs=DEFAULT_COEFFS,
+                stream=None) -> None:
+    """muon_step_static: one step with the library's static device scratch
+    instead of a caller-allocated workspace (for callers that cannot
+    allocate; plans needing more than STATIC_WORKSPACE_BYTES are rejected).
+    Calls that overlap on the GPU share, and race on, that scratch."""
+    c = (ctypes.c_float * 3)(*coeffs)
+    _check(load().muon_step_static(plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum), lr,
+                                   beta, wd, int(bool(nesterov)), ns_steps, c,
+                                   ctypes.c_void_p(_stream_handle(stream))), "muon_step_static")
 
 
 def workspace_error(workspace: torch.Tensor, stream=None, clear: bool = True) -> int:
