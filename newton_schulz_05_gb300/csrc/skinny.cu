@@ -12,22 +12,27 @@
 // GB300 design:
 //   * one thread-block cluster per slice, C CTAs (<= 8), one CTA per SM;
 //     CTA r owns a contiguous range of 32-column "superchunks" of the
-//     working matrix X [m, n] (m = min(M, N); X = V^T when M > N);
-//   * X lives in tensor memory (TMEM, 512 columns x 128 lanes x 4 B per SM)
-//     between passes: every lane keeps, per superchunk, 4 registers per
-//     8-row block in the layout of a warp-MMA fragment, so X never returns
-//     to HBM: HBM traffic is G + M (read), M' (write), W (read + write),
-//     14 bytes per element for bf16 parameters;
-//   * X X^T and B X run on the tensor cores as m16n8k16 / m16n8k8 fp16 warp
-//     MMAs with fp32 accumulation; B X needs X as the B operand, obtained
-//     with movmatrix transposes of the 8x8 register blocks;
-//   * the m x m Gram matrix is reduced deterministically: warps -> CTA in
-//     shared memory, CTAs -> cluster through distributed shared memory in
-//     rank order, so every CTA holds the same bits; A*A and B = b*A + c*A*A
-//     are computed in fp32 by every CTA;
-//   * the Frobenius norm is reduced the same way; V is kept as bf16 until
-//     the norm is known, then X0 = fp16(V / (||V|| + eps)).
-//   * W is prefetched into L2 (bulk prefetch) while the iteration runs.
+//     working matrix (m = min(M, N) rows; the slice is read transposed when
+//     M > N);
+//   * Newton-Schulz runs in Gram space (see skinny_kernel): one pass over
+//     the slice forms V V^T, the T steps act on m x m matrices only, a
+//     second pass applies O = Q X_0.  For m << n this removes 2(T-1) of the
+//     2T passes over the long dimension and their syncs;
+//   * between the passes V lives in tensor memory (TMEM, 512 columns x 128
+//     lanes x 4 B per SM), 4 registers per 8-row block per lane in the layout
+//     of a warp-MMA fragment, so the slice never returns to HBM: traffic is
+//     G + M read, M' written, W read and W' written, 14 B per element for
+//     bf16 parameters;
+//   * V V^T (bf16 operands) and Q X_0 (fp16 operands: X_0 is V times a power
+//     of two, exact) run on the tensor cores as m16n8k16 / m16n8k8 warp MMAs
+//     with fp32 accumulation; Q X_0 takes X_0 as its B operand through
+//     movmatrix transposes of the 8x8 register blocks;
+//   * ||V||^2 and V V^T are reduced deterministically: warps -> CTA in shared
+//     memory, CTAs -> cluster through distributed shared memory in rank
+//     order, so every CTA holds the same bits and computes the same Q in fp32;
+//   * gradient and momentum rows are prefetched into L2 a few superchunks
+//     ahead, the parameter rows while Q is being formed, and the parameter
+//     loads of the update are issued one superchunk ahead.
 #include <cooperative_groups.h>
 #include <cstdio>
 
@@ -48,6 +53,8 @@ struct SkinnyParams {
   int sc_per_cta, sc_per_warp;
   int cluster;
   int vec;           // vectorised global access allowed for every slice
+  int staged;        // rows stream through the shared-memory ring (bulk copies)
+  int* err;          // device error word (bounded waits)
   StepArgs st;
   float lrs;         // lr * scale
   float decay;       // 1 - lr * wd
@@ -113,6 +120,38 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// bounded wait for the phase of parity `parity`; false when the budget ran out
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < (1u << 26); ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+// one contiguous global -> shared copy, completion counted on `bar`
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // 4 consecutive working columns c..c+3 of working row i of one slice.
@@ -189,19 +228,42 @@ struct Access {
   }
 };
 
-template <int MB, int NW>
+template <int MB, int NW, int ES>
 struct SkinnySmem {
   static constexpr int MP = 8 * MB;
   static constexpr int NP = (MB + 1) / 2;
   static constexpr int MPX = 16 * NP;
-  static constexpr size_t gram_w = 0;
-  static constexpr size_t gram_c = gram_w + sizeof(float) * NW * MP * MP;
-  static constexpr size_t afull = gram_c + sizeof(float) * 2 * MP * MP;
-  static constexpr size_t bm = afull + sizeof(float) * MP * MP;
-  static constexpr size_t misc = (bm + sizeof(__half) * MPX * MPX + 15) & ~size_t(15);
+  static constexpr size_t MAT = sizeof(float) * MP * MP;
+  // ring of row stages (bulk copies): SW columns, one superchunk per warp;
+  // row pitches padded so the fragment reads of a warp hit distinct banks
+  static constexpr int SW = 32 * NW;
+  static constexpr int PITCH_G = SW * ES + (ES == 2 ? 32 : 64);
+  static constexpr int PITCH_M = SW * 4 + 64;
+  static constexpr size_t STAGE = (size_t)MP * (PITCH_G + PITCH_M);
+  static constexpr int FIT = (int)((212 * 1024) / STAGE);
+  static constexpr bool STAGED = MB <= 4 && FIT >= 2;
+  static constexpr int NSTAGE = !STAGED ? 0 : (FIT >= 4 ? 4 : FIT);
+  static constexpr size_t RING = STAGED ? NSTAGE * STAGE : 0;
+  // the warp partials and the m x m matrices reuse the ring between the two
+  // passes (NW >= 8 > 5 matrices)
+  static constexpr size_t ring = 0;
+  static constexpr size_t gram_w = 0;                       // NW warp partials
+  static constexpr size_t mat_a = 0;                        // A_t
+  static constexpr size_t mat_p = mat_a + MAT;              // P_t
+  static constexpr size_t mat_q = mat_p + MAT;              // Q_t = P_{t-1} ... P_0
+  static constexpr size_t mat_t1 = mat_q + MAT;             // scratch products
+  static constexpr size_t mat_t2 = mat_t1 + MAT;
+  static constexpr size_t region = RING > NW * MAT ? RING : NW * MAT;
+  static constexpr size_t gram_c = region;                  // CTA partial (cluster-visible)
+  static constexpr size_t qh = gram_c + MAT;                // fp16 Q, the MMA A operand
+  static constexpr size_t bars = (qh + sizeof(__half) * MPX * MPX + 15) & ~size_t(15);
+  static constexpr size_t misc = bars + 8 * 8 + 8 * 4;      // 8 mbarriers, 8 counters
   static constexpr size_t total = misc + 64 * sizeof(float) + 16;
   // one CTA per SM: a second CTA on the SM would wait for tensor memory
   static constexpr size_t launch = total > 120 * 1024 ? total : 120 * 1024;
+  static_assert(NW >= 5, "matrices alias the warp partials");
+  static_assert(!STAGED || NSTAGE >= 2, "ring depth");
+  static_assert(launch <= 227 * 1024, "shared memory");
 };
 
 // Gram tiles: rows 16P..16P+15 (row blocks 2P, 2P+1) x row block J, J >= 2P.
@@ -210,6 +272,16 @@ __device__ __forceinline__ bool gram_covered(int i, int j) {
   return J >= ((I >> 1) << 1);
 }
 
+__device__ __forceinline__ void mma_k16_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// X X^T partial of one superchunk (bf16 fragments, fp32 accumulation)
 template <int MB>
 __device__ __forceinline__ void gram_accum(float (&acc)[(MB + 1) / 2][MB][4],
                                            const uint32_t (&x)[MB][4]) {
@@ -222,24 +294,89 @@ __device__ __forceinline__ void gram_accum(float (&acc)[(MB + 1) / 2][MB][4],
       const uint32_t a1 = (2 * P + 1 < MB) ? x[(2 * P + 1) % MB][2 * k] : 0u;
       const uint32_t a3 = (2 * P + 1 < MB) ? x[(2 * P + 1) % MB][2 * k + 1] : 0u;
       #pragma unroll
-      for (int J = 2 * P; J < MB; ++J) mma_k16(acc[P][J], a0, a1, a2, a3, x[J][2 * k], x[J][2 * k + 1]);
+      for (int J = 2 * P; J < MB; ++J)
+        mma_k16_bf16(acc[P][J], a0, a1, a2, a3, x[J][2 * k], x[J][2 * k + 1]);
     }
 }
 
+// Register tile of the m x m products: TB x TB outputs per thread, (MP/TB)^2
+// threads busy, the smallest TB whose thread count fits the CTA.
+template <int MP, int NT>
+struct MatTile {
+  static constexpr int TB = (MP / 2) * (MP / 2) <= NT ? 2 : ((MP + 2) / 3) * ((MP + 2) / 3) <= NT ? 3 : 4;
+  static constexpr int NB = (MP + TB - 1) / TB;
+  static_assert(NB * NB <= NT, "tile");
+};
+
+// D[i][j] = sum_k A[i][k] B[k][j]  (+ fused P epilogue when MODE == 1:
+// D = c*(A A) + b*A + a*I, with B == A), MP x MP fp32 in shared memory.
+template <int MP, int NT, int MODE>
+__device__ __forceinline__ void mat_mul(float* D, const float* A, const float* B, int tid,
+                                        float a = 0.f, float b = 0.f, float c = 0.f) {
+  using T = MatTile<MP, NT>;
+  constexpr int TB = T::TB, NB = T::NB;
+  if (tid >= NB * NB) return;
+  const int i0 = (tid / NB) * TB, j0 = (tid % NB) * TB;
+  float acc[TB][TB];
+  #pragma unroll
+  for (int x = 0; x < TB; ++x)
+    #pragma unroll
+    for (int y = 0; y < TB; ++y) acc[x][y] = 0.f;
+  #pragma unroll 4
+  for (int k = 0; k < MP; ++k) {
+    float av[TB], bv[TB];
+    #pragma unroll
+    for (int x = 0; x < TB; ++x) av[x] = (i0 + x < MP) ? A[(i0 + x) * MP + k] : 0.f;
+    #pragma unroll
+    for (int y = 0; y < TB; ++y) bv[y] = (j0 + y < MP) ? B[k * MP + j0 + y] : 0.f;
+    #pragma unroll
+    for (int x = 0; x < TB; ++x)
+      #pragma unroll
+      for (int y = 0; y < TB; ++y) acc[x][y] = fmaf(av[x], bv[y], acc[x][y]);
+  }
+  #pragma unroll
+  for (int x = 0; x < TB; ++x)
+    #pragma unroll
+    for (int y = 0; y < TB; ++y) {
+      const int i = i0 + x, j = j0 + y;
+      if (i < MP && j < MP) {
+        float v = acc[x][y];
+        if (MODE == 1) v = fmaf(c, v, fmaf(b, A[i * MP + j], i == j ? a : 0.f));
+        D[i * MP + j] = v;
+      }
+    }
+}
+
+// The whole Muon step of one slice per cluster.
+//
+// Newton-Schulz in Gram space: with A_t = X_t X_t^T each step is
+// X_{t+1} = P_t X_t, P_t = a I + b A_t + c A_t^2, a polynomial in A_t, hence
+// symmetric and commuting with A_t, so A_{t+1} = P_t A_t P_t and
+// X_T = (P_{T-1} ... P_0) X_0 = Q X_0.  The iteration is thus carried out
+// exactly on m x m matrices: one pass over the slice forms A_0, the m x m
+// recursion gives Q, one more pass applies O = Q X_0.
 template <int MB, int NW, typename PT>
 __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constant__ SkinnyParams p) {
-  using S = SkinnySmem<MB, NW>;
+  using S = SkinnySmem<MB, NW, (int)sizeof(PT)>;
   constexpr int MP = S::MP, NP = S::NP, MPX = S::MPX;
   constexpr int NT = NW * 32;
   constexpr int COLS_W = 512 / (NW / 4);
+  constexpr int LOOKAHEAD = 3;   // superchunks prefetched into L2 ahead of use (direct path)
+  constexpr int NSTG = S::NSTAGE > 0 ? S::NSTAGE : 1;
   extern __shared__ __align__(128) unsigned char smem[];
   float* gram_w = reinterpret_cast<float*>(smem + S::gram_w);
   float* gram_c = reinterpret_cast<float*>(smem + S::gram_c);
-  float* afull = reinterpret_cast<float*>(smem + S::afull);
-  __half* bm = reinterpret_cast<__half*>(smem + S::bm);
+  float* mA = reinterpret_cast<float*>(smem + S::mat_a);
+  float* mP = reinterpret_cast<float*>(smem + S::mat_p);
+  float* mQ = reinterpret_cast<float*>(smem + S::mat_q);
+  float* mT1 = reinterpret_cast<float*>(smem + S::mat_t1);
+  float* mT2 = reinterpret_cast<float*>(smem + S::mat_t2);
+  __half* qh = reinterpret_cast<__half*>(smem + S::qh);
   float* red = reinterpret_cast<float*>(smem + S::misc);     // NW floats
   float* norm_slot = red + 32;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 48);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::bars);  // stage landed
+  int* done_cnt = reinterpret_cast<int*>(smem + S::bars + 64);     // warps done with a stage
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -253,7 +390,12 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   float* Oout = p.ptrs.O[slice];
   const StepArgs& st = p.st;
 
-  for (int e = tid; e < MPX * MPX; e += NT) bm[e] = __float2half_rn(0.f);
+  for (int e = tid; e < MPX * MPX; e += NT) qh[e] = __float2half_rn(0.f);
+  const bool staged = S::STAGED && p.staged;
+  if (tid == 0) {
+    for (int b = 0; b < 8; ++b) { mbar_init(&full[b], 1); done_cnt[b] = 0; }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
                      smem_u32(tmem_slot))
@@ -266,24 +408,126 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   const uint32_t tbase = *tmem_slot;
   const uint32_t taddr_w = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * COLS_W);
 
+  // slot q of warp w is superchunk jc0 + w + q*NW: at any moment the CTA's
+  // warps stream one contiguous stretch of every row
   const int jc0 = rank * p.sc_per_cta;
   const int jc1 = min(p.nsc, jc0 + p.sc_per_cta);
-  const int j0 = jc0 + warp * p.sc_per_warp;
-  const int j1 = min(jc1, j0 + p.sc_per_warp);
-  const int nslot = max(0, j1 - j0);
+  const int nslot = max(0, (jc1 - jc0 - warp + NW - 1) / NW);
+  auto sc_col = [&](int q) { return (jc0 + warp + q * NW) * 32; };
 
-  // ---- phase 1: momentum, V (bf16 in TMEM), sum of squares -------------------
-  float ss = 0.f;
-  for (int q = 0; q < nslot; ++q) {
-    const int cb = (j0 + q) * 32;
-    float gv[MB][2][4], mv[MB][2][4];
-    #pragma unroll
-    for (int rb = 0; rb < MB; ++rb)
-      #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        acc_.template load<true>(G, rb * 8 + g, cb + h * 16 + 4 * t4, gv[rb][h]);
-        acc_.load_f32(Mo, rb * 8 + g, cb + h * 16 + 4 * t4, mv[rb][h]);
+  const int c_lo = jc0 * 32, c_hi = min(p.n, jc1 * 32);
+  const int nstage = jc1 > jc0 ? (c_hi - c_lo + S::SW - 1) / S::SW : 0;   // stages per pass
+  bool wait_ok = true;
+  // stage k < nstage: G and M rows of columns [c_lo + k*SW, ...);
+  // stage k >= nstage: W rows of stage k - nstage.  One thread issues it.
+  auto issue_stage = [&](int k) {
+    if (!S::STAGED) return;
+    const int b = k % NSTG;
+    const int s2 = k < nstage ? k : k - nstage;
+    const int c0 = c_lo + s2 * S::SW;
+    const int cols = min(S::SW, c_hi - c0);
+    unsigned char* base = smem + S::ring + (size_t)b * S::STAGE;
+    if (k < nstage) {
+      mbar_expect_tx(&full[b], (uint32_t)(p.m * cols * ((int)sizeof(PT) + 4)));
+      for (int i = 0; i < p.m; ++i) {
+        bulk_load(base + i * S::PITCH_G, G + (size_t)i * p.n + c0, cols * (int)sizeof(PT), &full[b]);
+        bulk_load(base + MP * S::PITCH_G + i * S::PITCH_M, Mo + (size_t)i * p.n + c0, cols * 4, &full[b]);
       }
+    } else {
+      mbar_expect_tx(&full[b], (uint32_t)(p.m * cols * (int)sizeof(PT)));
+      for (int i = 0; i < p.m; ++i)
+        bulk_load(base + i * S::PITCH_G, W + (size_t)i * p.n + c0, cols * (int)sizeof(PT), &full[b]);
+    }
+  };
+  // a warp is done with stage k: the last one refills its buffer with stage
+  // k + NSTAGE of the same pass
+  auto release_stage = [&](int k, int k_end) {
+    __syncwarp();
+    if (lane == 0) {
+      const int b = k % NSTG;
+      __threadfence_block();
+      if (atomicAdd(&done_cnt[b], 1) == NW - 1) {
+        done_cnt[b] = 0;
+        if (k + NSTG < k_end) {
+          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+          issue_stage(k + NSTG);
+        }
+      }
+    }
+  };
+  auto stage_wait = [&](int k) {
+    if (!mbar_wait(&full[k % NSTG], (uint32_t)((k / NSTG) & 1)) && wait_ok) {
+      wait_ok = false;
+      atomicExch(p.err, kDevErrTimeout);
+    }
+  };
+  // L2 prefetch of one superchunk's gradient and momentum rows (direct path)
+  auto prefetch_sc = [&](int q) {
+    if (staged || !p.vec || q >= nslot) return;
+    const int cb = sc_col(q);
+    for (int i = lane; i < p.m; i += 32) {
+      const size_t off = (size_t)i * p.n + cb;
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(G + off));
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(Mo + off));
+    }
+  };
+  if (staged && tid == 0)
+    for (int k = 0; k < min(NSTG, nstage); ++k) issue_stage(k);
+  for (int q = 0; q < LOOKAHEAD; ++q) prefetch_sc(q);
+
+  // ---- pass 1: momentum, V (bf16 in TMEM), sum of squares, Gram of V ----------
+  float ss = 0.f;
+  float gacc[NP][MB][4];
+  #pragma unroll
+  for (int P = 0; P < NP; ++P)
+    #pragma unroll
+    for (int J = 0; J < MB; ++J)
+      #pragma unroll
+      for (int e = 0; e < 4; ++e) gacc[P][J][e] = 0.f;
+  const int npass = staged ? nstage : nslot;
+  for (int q = 0; q < npass; ++q) {
+    const bool has = q < nslot;       // warp has a superchunk in this stage
+    float gv[MB][2][4], mv[MB][2][4];
+    if (staged) {
+      stage_wait(q);
+      const unsigned char* base = smem + S::ring + (size_t)(q % NSTG) * S::STAGE;
+      #pragma unroll
+      for (int rb = 0; rb < MB; ++rb)
+        #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = rb * 8 + g;
+          const int cl = warp * 32 + h * 16 + 4 * t4;   // column inside the stage
+          const bool in = has && i < p.m && sc_col(q) + h * 16 + 4 * t4 < p.n;
+          if (in) {
+            if constexpr (sizeof(PT) == 2) {
+              const uint2 u = *reinterpret_cast<const uint2*>(base + i * S::PITCH_G + cl * 2);
+              const float2 x = unpack_bf16(u.x), y = unpack_bf16(u.y);
+              gv[rb][h][0] = x.x; gv[rb][h][1] = x.y; gv[rb][h][2] = y.x; gv[rb][h][3] = y.y;
+            } else {
+              const float4 u = *reinterpret_cast<const float4*>(base + i * S::PITCH_G + cl * 4);
+              gv[rb][h][0] = u.x; gv[rb][h][1] = u.y; gv[rb][h][2] = u.z; gv[rb][h][3] = u.w;
+            }
+            const float4 u = *reinterpret_cast<const float4*>(base + MP * S::PITCH_G + i * S::PITCH_M + cl * 4);
+            mv[rb][h][0] = u.x; mv[rb][h][1] = u.y; mv[rb][h][2] = u.z; mv[rb][h][3] = u.w;
+          } else {
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) gv[rb][h][e] = mv[rb][h][e] = 0.f;
+          }
+        }
+      release_stage(q, nstage);
+    } else {
+      prefetch_sc(q + LOOKAHEAD);
+      const int cb = sc_col(q);
+      #pragma unroll
+      for (int rb = 0; rb < MB; ++rb)
+        #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          acc_.template load<true>(G, rb * 8 + g, cb + h * 16 + 4 * t4, gv[rb][h]);
+          acc_.load_f32(Mo, rb * 8 + g, cb + h * 16 + 4 * t4, mv[rb][h]);
+        }
+    }
+    if (!has) continue;
+    const int cb = sc_col(q);
     uint32_t xr[MB][4];
     #pragma unroll
     for (int rb = 0; rb < MB; ++rb)
@@ -303,23 +547,8 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
       }
     #pragma unroll
     for (int rb = 0; rb < MB; ++rb) tm_st4(taddr_w + q * 4 * MB + 4 * rb, xr[rb]);
+    gram_accum<MB>(gacc, xr);
   }
-  tm_wait_st();
-
-  // ---- cluster-wide ||V||_F (fixed order) ------------------------------------
-  #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) red[warp] = ss;
-  __syncthreads();
-  if (tid == 0) {
-    float s = 0.f;
-    for (int w = 0; w < NW; ++w) s += red[w];
-    norm_slot[0] = s;
-  }
-  cluster.sync();
-  float tot = 0.f;
-  for (int r = 0; r < p.cluster; ++r) tot += *cluster.map_shared_rank(norm_slot, r);
-  const float inv = 1.f / (sqrtf(tot) + st.eps);
 
   // warm L2 with this CTA's parameter rows for the final update
   if (warp == NW - 1 && jc1 > jc0) {
@@ -339,177 +568,196 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     }
   }
 
-  auto epilogue = [&](int q, const float (&o)[MB][4][2]) {
-    const int cb = (j0 + q) * 32;
+  // ---- cluster-wide ||V||^2 and V V^T (fixed order: warps, then ranks) -----------
+  __syncthreads();   // the warp partials reuse the ring
+  {
+    float* gw = gram_w + warp * MP * MP;
+    #pragma unroll
+    for (int P = 0; P < NP; ++P)
+      #pragma unroll
+      for (int J = 2 * P; J < MB; ++J)
+        #pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int row = 16 * P + 8 * hh + g;
+          if (row < MP) {
+            gw[row * MP + 8 * J + 2 * t4] = gacc[P][J][2 * hh];
+            gw[row * MP + 8 * J + 2 * t4 + 1] = gacc[P][J][2 * hh + 1];
+          }
+        }
+  }
+  #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[warp] = ss;
+  tm_wait_st();
+  __syncthreads();
+  for (int e = tid; e < MP * MP; e += NT) {
+    if (!gram_covered(e / MP, e % MP)) continue;
+    float s = 0.f;
+    for (int w = 0; w < NW; ++w) s += gram_w[w * MP * MP + e];
+    gram_c[e] = s;
+  }
+  if (tid == 0) {
+    float s = 0.f;
+    for (int w = 0; w < NW; ++w) s += red[w];
+    norm_slot[0] = s;
+  }
+  cluster.sync();
+  float tot = 0.f;
+  for (int r = 0; r < p.cluster; ++r) tot += *cluster.map_shared_rank(norm_slot, r);
+  const float inv = 1.f / (sqrtf(tot) + st.eps);
+  // X0 = V * 2^-e exactly (power of two near 1/||V||): bf16 -> fp16 loses nothing
+  int ex = 0;
+  frexpf(sqrtf(tot), &ex);
+  const float sp = ldexpf(1.f, -ex);
+  for (int e = tid; e < MP * MP; e += NT) {
+    const int i = e / MP, j = e % MP;
+    const int src = gram_covered(i, j) ? e : j * MP + i;
+    float s = 0.f;
+    for (int r = 0; r < p.cluster; ++r) s += cluster.map_shared_rank(gram_c, r)[src];
+    mA[e] = s * inv * inv;                        // A_0 = X_0 X_0^T
+    mQ[e] = i == j ? 1.f : 0.f;
+  }
+  __syncthreads();
+
+  // ---- m x m recursion: P_t = aI + bA_t + cA_t^2;  Q <- P_t Q;  A <- P_t A_t P_t ----
+  for (int t = 0; t < st.T; ++t) {
+    mat_mul<MP, NT, 1>(mP, mA, mA, tid, st.a, st.b, st.c);   // P = aI + bA + cA^2
+    __syncthreads();
+    mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);                      // Q <- P Q
+    if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid);    // P A
+    __syncthreads();
+    { float* x = mQ; mQ = mT1; mT1 = x; }
+    if (t + 1 < st.T) {
+      mat_mul<MP, NT, 0>(mA, mT2, mP, tid);                    // A <- (P A) P
+      __syncthreads();
+    }
+  }
+  // O = Q X_0 = (Q * inv / sp) (V * sp); the fp16 operand is the scaled Q
+  const float qscale = tot > 0.f ? inv / sp : 0.f;
+  for (int e = tid; e < MP * MP; e += NT) {
+    const int i = e / MP, j = e % MP;
+    qh[i * MPX + j] = __float2half_rn(mQ[e] * qscale);
+  }
+  __syncthreads();
+  uint32_t afr[NP][NP][4];
+  #pragma unroll
+  for (int P = 0; P < NP; ++P)
+    #pragma unroll
+    for (int kk = 0; kk < NP; ++kk) {
+      const __half* r0 = qh + (16 * P + g) * MPX + 16 * kk + 2 * t4;
+      const __half* r1 = r0 + 8 * MPX;
+      afr[P][kk][0] = *reinterpret_cast<const uint32_t*>(r0);
+      afr[P][kk][1] = *reinterpret_cast<const uint32_t*>(r1);
+      afr[P][kk][2] = *reinterpret_cast<const uint32_t*>(r0 + 8);
+      afr[P][kk][3] = *reinterpret_cast<const uint32_t*>(r1 + 8);
+    }
+
+  // ---- pass 2: O = Q X_0 and W' = W (1 - lr wd) - lr s O -------------------------
+  // (the ring held the m x m matrices until the barrier above)
+  if (staged && tid == 0) {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    for (int k = 0; k < min(NSTG, nstage); ++k) issue_stage(nstage + k);
+  }
+  float wbuf[MB][2][4];
+  auto load_w = [&](int q) {
+    const int cb = sc_col(q);
+    #pragma unroll
+    for (int rb = 0; rb < MB; ++rb)
+      #pragma unroll
+      for (int h = 0; h < 2; ++h)
+        acc_.template load<false>(W, rb * 8 + g, cb + h * 16 + 4 * t4, wbuf[rb][h]);
+  };
+  if (!staged && nslot > 0) load_w(0);
+  for (int q = 0; q < npass; ++q) {
+    const bool has = q < nslot;
+    uint32_t xr[MB][4];
+    if (has) {
+      #pragma unroll
+      for (int rb = 0; rb < MB; ++rb) tm_ld4(taddr_w + q * 4 * MB + 4 * rb, xr[rb]);
+    }
+    float wcur[MB][2][4];
+    if (staged) {
+      stage_wait(nstage + q);
+      const unsigned char* base = smem + S::ring + (size_t)((nstage + q) % NSTG) * S::STAGE;
+      #pragma unroll
+      for (int rb = 0; rb < MB; ++rb)
+        #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = rb * 8 + g;
+          const int cl = warp * 32 + h * 16 + 4 * t4;
+          const bool in = has && i < p.m && sc_col(q) + h * 16 + 4 * t4 < p.n;
+          if (in) {
+            if constexpr (sizeof(PT) == 2) {
+              const uint2 u = *reinterpret_cast<const uint2*>(base + i * S::PITCH_G + cl * 2);
+              const float2 x = unpack_bf16(u.x), y = unpack_bf16(u.y);
+              wcur[rb][h][0] = x.x; wcur[rb][h][1] = x.y; wcur[rb][h][2] = y.x; wcur[rb][h][3] = y.y;
+            } else {
+              const float4 u = *reinterpret_cast<const float4*>(base + i * S::PITCH_G + cl * 4);
+              wcur[rb][h][0] = u.x; wcur[rb][h][1] = u.y; wcur[rb][h][2] = u.z; wcur[rb][h][3] = u.w;
+            }
+          } else {
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) wcur[rb][h][e] = 0.f;
+          }
+        }
+      release_stage(nstage + q, 2 * nstage);
+    } else {
+      #pragma unroll
+      for (int rb = 0; rb < MB; ++rb)
+        #pragma unroll
+        for (int h = 0; h < 2; ++h)
+          #pragma unroll
+          for (int e = 0; e < 4; ++e) wcur[rb][h][e] = wbuf[rb][h][e];
+      if (q + 1 < nslot) load_w(q + 1);
+    }
+    if (!has) continue;
+    tm_wait_ld();
+    #pragma unroll
+    for (int rb = 0; rb < MB; ++rb)
+      #pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float2 f = unpack_bf16(xr[rb][r]);
+        xr[rb][r] = pack_h(f.x * sp, f.y * sp);
+      }
+    float o[MB][4][2];
+    #pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      uint32_t xt[MB];
+      #pragma unroll
+      for (int J = 0; J < MB; ++J) xt[J] = movt(xr[J][r]);
+      #pragma unroll
+      for (int P = 0; P < NP; ++P) {
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        #pragma unroll
+        for (int kk = 0; kk < NP; ++kk) {
+          if (2 * kk + 1 < MB)
+            mma_k16(y, afr[P][kk][0], afr[P][kk][1], afr[P][kk][2], afr[P][kk][3], xt[2 * kk],
+                    xt[(2 * kk + 1) % MB]);
+          else
+            mma_k8(y, afr[P][kk][0], afr[P][kk][1], xt[2 * kk]);
+        }
+        o[2 * P][r][0] = y[0];
+        o[2 * P][r][1] = y[1];
+        if (2 * P + 1 < MB) {
+          o[(2 * P + 1) % MB][r][0] = y[2];
+          o[(2 * P + 1) % MB][r][1] = y[3];
+        }
+      }
+    }
+    const int cb = sc_col(q);
     #pragma unroll
     for (int rb = 0; rb < MB; ++rb)
       #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int i = rb * 8 + g, c = cb + h * 16 + 4 * t4;
-        float w[4];
-        acc_.template load<false>(W, i, c, w);
         const float ov[4] = {o[rb][2 * h][0], o[rb][2 * h][1], o[rb][2 * h + 1][0],
                              o[rb][2 * h + 1][1]};
         float wn[4];
         #pragma unroll
-        for (int e = 0; e < 4; ++e) wn[e] = fmaf(w[e], p.decay, -p.lrs * ov[e]);
+        for (int e = 0; e < 4; ++e) wn[e] = fmaf(wcur[rb][h][e], p.decay, -p.lrs * ov[e]);
         acc_.store(W, i, c, wn);
         if (Oout) acc_.store_f32(Oout, i, c, ov);
       }
-  };
-
-  if (st.T == 0) {
-    // O = V / (||V|| + eps)
-    for (int q = 0; q < nslot; ++q) {
-      uint32_t xr[MB][4];
-      #pragma unroll
-      for (int rb = 0; rb < MB; ++rb) tm_ld4(taddr_w + q * 4 * MB + 4 * rb, xr[rb]);
-      tm_wait_ld();
-      float o[MB][4][2];
-      #pragma unroll
-      for (int rb = 0; rb < MB; ++rb)
-        #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const float2 f = unpack_bf16(xr[rb][r]);
-          o[rb][r][0] = f.x * inv;
-          o[rb][r][1] = f.y * inv;
-        }
-      epilogue(q, o);
-    }
-  } else {
-    // ---- phase 2: X0 = fp16(V * inv) and its Gram partial --------------------
-    float gacc[NP][MB][4];
-    #pragma unroll
-    for (int P = 0; P < NP; ++P)
-      #pragma unroll
-      for (int J = 0; J < MB; ++J)
-        #pragma unroll
-        for (int e = 0; e < 4; ++e) gacc[P][J][e] = 0.f;
-    for (int q = 0; q < nslot; ++q) {
-      uint32_t xr[MB][4];
-      #pragma unroll
-      for (int rb = 0; rb < MB; ++rb) tm_ld4(taddr_w + q * 4 * MB + 4 * rb, xr[rb]);
-      tm_wait_ld();
-      #pragma unroll
-      for (int rb = 0; rb < MB; ++rb)
-        #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const float2 f = unpack_bf16(xr[rb][r]);
-          xr[rb][r] = pack_h(f.x * inv, f.y * inv);
-        }
-      #pragma unroll
-      for (int rb = 0; rb < MB; ++rb) tm_st4(taddr_w + q * 4 * MB + 4 * rb, xr[rb]);
-      gram_accum<MB>(gacc, xr);
-    }
-    tm_wait_st();
-
-    for (int t = 0; t < st.T; ++t) {
-      const bool last = t == st.T - 1;
-      // warp partial -> shared memory
-      float* gw = gram_w + warp * MP * MP;
-      #pragma unroll
-      for (int P = 0; P < NP; ++P)
-        #pragma unroll
-        for (int J = 2 * P; J < MB; ++J)
-          #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int row = 16 * P + 8 * hh + g;
-            if (row < MP) {
-              gw[row * MP + 8 * J + 2 * t4] = gacc[P][J][2 * hh];
-              gw[row * MP + 8 * J + 2 * t4 + 1] = gacc[P][J][2 * hh + 1];
-            }
-          }
-      __syncthreads();
-      float* gc = gram_c + (t & 1) * MP * MP;
-      for (int e = tid; e < MP * MP; e += NT) {
-        if (!gram_covered(e / MP, e % MP)) continue;
-        float s = 0.f;
-        for (int w = 0; w < NW; ++w) s += gram_w[w * MP * MP + e];
-        gc[e] = s;
-      }
-      cluster.sync();
-      for (int e = tid; e < MP * MP; e += NT) {
-        const int i = e / MP, j = e % MP;
-        const int src = gram_covered(i, j) ? e : j * MP + i;
-        float s = 0.f;
-        for (int r = 0; r < p.cluster; ++r) s += cluster.map_shared_rank(gc, r)[src];
-        afull[e] = s;
-      }
-      __syncthreads();
-      for (int e = tid; e < MP * MP; e += NT) {
-        const int i = e / MP, j = e % MP;
-        float s = 0.f;
-        #pragma unroll 8
-        for (int k = 0; k < MP; ++k) s = fmaf(afull[i * MP + k], afull[k * MP + j], s);
-        bm[i * MPX + j] = __float2half_rn(fmaf(st.b, afull[e], st.c * s));
-      }
-      __syncthreads();
-      // B as the A operand of Y = B X: rows 16P.., k steps over row-block pairs
-      uint32_t afr[NP][NP][4];
-      #pragma unroll
-      for (int P = 0; P < NP; ++P)
-        #pragma unroll
-        for (int kk = 0; kk < NP; ++kk) {
-          const __half* r0 = bm + (16 * P + g) * MPX + 16 * kk + 2 * t4;
-          const __half* r1 = r0 + 8 * MPX;
-          afr[P][kk][0] = *reinterpret_cast<const uint32_t*>(r0);
-          afr[P][kk][1] = *reinterpret_cast<const uint32_t*>(r1);
-          afr[P][kk][2] = *reinterpret_cast<const uint32_t*>(r0 + 8);
-          afr[P][kk][3] = *reinterpret_cast<const uint32_t*>(r1 + 8);
-        }
-      if (!last) {
-        #pragma unroll
-        for (int P = 0; P < NP; ++P)
-          #pragma unroll
-          for (int J = 0; J < MB; ++J)
-            #pragma unroll
-            for (int e = 0; e < 4; ++e) gacc[P][J][e] = 0.f;
-      }
-      for (int q = 0; q < nslot; ++q) {
-        uint32_t xr[MB][4];
-        #pragma unroll
-        for (int rb = 0; rb < MB; ++rb) tm_ld4(taddr_w + q * 4 * MB + 4 * rb, xr[rb]);
-        tm_wait_ld();
-        float o[MB][4][2];
-        #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          uint32_t xt[MB];
-          #pragma unroll
-          for (int J = 0; J < MB; ++J) xt[J] = movt(xr[J][r]);
-          float y[NP][4];
-          #pragma unroll
-          for (int P = 0; P < NP; ++P) {
-            y[P][0] = y[P][1] = y[P][2] = y[P][3] = 0.f;
-            #pragma unroll
-            for (int kk = 0; kk < NP; ++kk) {
-              if (2 * kk + 1 < MB)
-                mma_k16(y[P], afr[P][kk][0], afr[P][kk][1], afr[P][kk][2], afr[P][kk][3],
-                        xt[2 * kk], xt[(2 * kk + 1) % MB]);
-              else
-                mma_k8(y[P], afr[P][kk][0], afr[P][kk][1], xt[2 * kk]);
-            }
-          }
-          #pragma unroll
-          for (int rb = 0; rb < MB; ++rb) {
-            const float2 x = unpack_h(xr[rb][r]);
-            o[rb][r][0] = fmaf(st.a, x.x, y[rb >> 1][(rb & 1) * 2]);
-            o[rb][r][1] = fmaf(st.a, x.y, y[rb >> 1][(rb & 1) * 2 + 1]);
-          }
-        }
-        if (last) {
-          epilogue(q, o);
-        } else {
-          #pragma unroll
-          for (int rb = 0; rb < MB; ++rb)
-            #pragma unroll
-            for (int r = 0; r < 4; ++r) xr[rb][r] = pack_h(o[rb][r][0], o[rb][r][1]);
-          #pragma unroll
-          for (int rb = 0; rb < MB; ++rb) tm_st4(taddr_w + q * 4 * MB + 4 * rb, xr[rb]);
-          gram_accum<MB>(gacc, xr);
-        }
-      }
-      tm_wait_st();
-    }
   }
   // no CTA may leave while a cluster peer can still read its shared memory
   tc_fence_before();
@@ -522,7 +770,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
 template <int MB, typename PT>
 cudaError_t launch_mb(const Group& g, const SkinnyParams& prm, int nslices, cudaStream_t s) {
   constexpr int NW = MB <= 4 ? 16 : 8;
-  using S = SkinnySmem<MB, NW>;
+  using S = SkinnySmem<MB, NW, (int)sizeof(PT)>;
   auto kern = skinny_kernel<MB, NW, PT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::launch);
@@ -558,7 +806,7 @@ cudaError_t launch_pt(const Group& g, const SkinnyParams& prm, int ns, cudaStrea
 }  // namespace
 
 cudaError_t launch_skinny(const Group& g, const SlicePtrs& ptrs, int nslices, const StepArgs& st,
-                          int* /*err_word*/, cudaStream_t s) {
+                          int* err_word, cudaStream_t s) {
   SkinnyParams prm;
   prm.ptrs = ptrs;
   prm.m = (int)g.m;
@@ -580,6 +828,16 @@ cudaError_t launch_skinny(const Group& g, const SlicePtrs& ptrs, int nslices, co
     if (ptrs.O[i] && reinterpret_cast<uintptr_t>(ptrs.O[i]) % 16) vec = 0;
   }
   prm.vec = vec;
+  // the ring needs 16-byte aligned row starts: rows of a multiple of 8
+  // elements and 16-byte aligned slice bases
+  int staged = (vec && g.n % 8 == 0 && g.mb <= 4) ? 1 : 0;
+  for (int i = 0; i < nslices && staged; ++i) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptrs.W[i]) | reinterpret_cast<uintptr_t>(ptrs.G[i]) |
+                        reinterpret_cast<uintptr_t>(ptrs.Mom[i]);
+    if (a % 16) staged = 0;
+  }
+  prm.staged = staged;
+  prm.err = err_word;
   if (g.dtype == MUON_BF16) return launch_pt<__nv_bfloat16>(g, prm, nslices, s);
   return launch_pt<float>(g, prm, nslices, s);
 }

@@ -106,6 +106,10 @@ WORKLOADS = {
     # synthetic MoE model, about 3.7 B parameters
     "moe_24L": Workload(
         "moe_24L", _moe_layers(24), torch.bfloat16, grad_std=1e-2),
+    # one expert stack of the MoE model: the small dense case used for
+    # kernel profiles (about 1.2 GB on the device with its workspace)
+    "experts_16x1408x2048": Workload(
+        "experts_16x1408x2048", ((16, 1408, 2048),), torch.bfloat16, grad_std=1e-2),
 }
 
 
