@@ -155,6 +155,26 @@ MUON_API muon_status muon_step_ortho(const muon_plan_t* plan, void* const* param
                             size_t ws_bytes, void* stream, float* const* ortho);
 
 /*
+ * muon_step on loss-scaled gradients (mixed-precision training with a loss
+ * scaler; the Paddle Muon sharding PR's review of its AMP GradScaler path
+ * shows the Muon step running behind such a scaler).
+ *   grads hold S * G for a loss scale S; the step uses G = grads * inv_scale
+ *   (the multiply is fused into the momentum update, no extra pass).
+ *   found_inf: device int.  Before any state changes, every gradient value of
+ *   every parameter is checked; *found_inf is set to 1 when one is inf or NaN,
+ *   and then no parameter and no momentum is modified (the step is skipped),
+ *   else *found_inf is set to 0 and the step runs.  The check reads every
+ *   gradient once more (2 bytes per bf16 element).
+ * inv_scale must be finite.  Other arguments are those of muon_step.
+ */
+MUON_API muon_status muon_step_amp(const muon_plan_t* plan, void* const* params,
+                                   const void* const* grads, float* const* momentum,
+                                   float lr, float beta, float wd, int nesterov,
+                                   int ns_steps, const float* coeffs, float inv_scale,
+                                   int* found_inf, void* workspace, size_t ws_bytes,
+                                   void* stream);
+
+/*
  * Read the device error word of a workspace after synchronising `stream`.
  * *code receives MUON_OK or the first device-side error recorded
  * (MUON_ERR_DEVICE_TIMEOUT); when clear != 0 the word is reset to zero.

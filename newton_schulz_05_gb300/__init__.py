@@ -57,7 +57,8 @@ class _GroupInfo(ctypes.Structure):
 EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
            "muon_plan_num_groups", "muon_plan_num_slices", "muon_plan_group",
            "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
-           "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static"]
+           "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static",
+           "muon_step_amp"]
 
 STATIC_WORKSPACE_BYTES = 32 << 20   # MUON_STATIC_WORKSPACE_BYTES in include/muon.h
 
@@ -89,6 +90,7 @@ def load(path: str = LIB_PATH):
     L.muon_step.argtypes = step_args
     L.muon_step_ortho.argtypes = step_args + [PP]
     L.muon_step_static.argtypes = step_args[:10] + [vp]
+    L.muon_step_amp.argtypes = step_args[:10] + [ctypes.c_float, vp, vp, sz, vp]
     L.muon_workspace_error.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.muon_plan_launches.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.muon_plan_destroy.argtypes = [vp]
@@ -98,7 +100,7 @@ def load(path: str = LIB_PATH):
     for fn in ("muon_plan", "muon_plan_workspace_bytes", "muon_plan_num_groups",
                "muon_plan_num_slices", "muon_plan_group", "muon_plan_slice", "muon_step",
                "muon_step_ortho", "muon_workspace_error", "muon_plan_launches",
-               "muon_step_static"):
+               "muon_step_static", "muon_step_amp"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -250,6 +252,23 @@ def step_static(plan: Plan, params, grads, momentum, *, lr: float, beta: float, 
     _check(load().muon_step_static(plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum), lr,
                                    beta, wd, int(bool(nesterov)), ns_steps, c,
                                    ctypes.c_void_p(_stream_handle(stream))), "muon_step_static")
+
+
+def step_amp(plan: Plan, params, grads, momentum, *, lr: float, beta: float, wd: float,
+             inv_scale: float, found_inf: torch.Tensor, nesterov: bool = True, ns_steps: int = 5,
+             coeffs=DEFAULT_COEFFS, workspace: torch.Tensor, stream=None) -> None:
+    """muon_step_amp: one step on loss-scaled gradients (grads * inv_scale),
+    skipped entirely when any gradient value is inf or NaN; found_inf is a
+    one-element int32 CUDA tensor that receives 1 (skipped) or 0."""
+    if found_inf.dtype != torch.int32 or not found_inf.is_cuda or found_inf.numel() < 1:
+        raise ValueError("found_inf must be a CUDA int32 tensor")
+    c = (ctypes.c_float * 3)(*coeffs)
+    _check(load().muon_step_amp(plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum), lr,
+                                beta, wd, int(bool(nesterov)), ns_steps, c, inv_scale,
+                                ctypes.c_void_p(found_inf.data_ptr()),
+                                ctypes.c_void_p(workspace.data_ptr()),
+                                workspace.numel() * workspace.element_size(),
+                                ctypes.c_void_p(_stream_handle(stream))), "muon_step_amp")
 
 
 def workspace_error(workspace: torch.Tensor, stream=None, clear: bool = True) -> int:

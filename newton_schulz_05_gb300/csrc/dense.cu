@@ -39,11 +39,34 @@ struct DenseBufs {
   float* inv;      // per-slice 1/(||V|| + eps)
 };
 
+__device__ __forceinline__ void load4(const float* p, float* v) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float* v) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+__device__ __forceinline__ void store4(float* p, const float* v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float* v) {
+  uint2 u;
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// vec: every slice's rows start 16-byte aligned (n % 4 == 0, aligned bases)
 template <typename PT>
 __global__ void __launch_bounds__(kNT) front_kernel(
     const __grid_constant__ SlicePtrs ptrs, int64_t m, int64_t n, int64_t m_pad,
-    int64_t n_pad, int tr, float beta, int nesterov, char* ws, size_t slice_ws,
-    size_t off_V, size_t off_part) {
+    int64_t n_pad, int tr, int vec, float beta, int nesterov, float gscale, const int* skip,
+    char* ws, size_t slice_ws, size_t off_V, size_t off_part) {
+  if (skip && *skip) return;   // skipped loss-scaled step: momentum untouched
   const int s = blockIdx.y;
   const int tiles_c = (int)(n_pad / kFrontTileC);
   const int64_t i0 = (int64_t)(blockIdx.x / tiles_c) * kFrontTileR;
@@ -57,7 +80,30 @@ __global__ void __launch_bounds__(kNT) front_kernel(
   __shared__ float tile[kFrontTileC][kFrontTileR + 1];
   float ss = 0.f;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (!tr) {
+  if (!tr && vec) {
+    // working (i, k) = stored (i, k); 4 consecutive elements per thread
+    for (int r = warp; r < kFrontTileR; r += kNT / 32) {
+      const int64_t i = i0 + r;
+      const int64_t k = k0 + 4 * lane;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (i < m && k < n) {
+        const int64_t idx = i * n + k;
+        float g[4], mo[4];
+        load4(G + idx, g);
+        const float4 mm4 = *reinterpret_cast<const float4*>(Mo + idx);
+        mo[0] = mm4.x; mo[1] = mm4.y; mo[2] = mm4.z; mo[3] = mm4.w;
+        #pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          g[e] *= gscale;
+          mo[e] = fmaf(beta, mo[e], g[e]);
+          v[e] = nesterov ? fmaf(beta, mo[e], g[e]) : mo[e];
+          ss = fmaf(v[e], v[e], ss);
+        }
+        *reinterpret_cast<float4*>(Mo + idx) = make_float4(mo[0], mo[1], mo[2], mo[3]);
+      }
+      *reinterpret_cast<float4*>(V + i * n_pad + k) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  } else if (!tr) {
     // working (i, k) = stored (i, k); stored slice is [m, n]
     for (int r = warp; r < kFrontTileR; r += kNT / 32) {
       const int64_t i = i0 + r;
@@ -66,7 +112,7 @@ __global__ void __launch_bounds__(kNT) front_kernel(
         float v = 0.f;
         if (i < m && k < n) {
           const int64_t idx = i * n + k;
-          const float g = to_f(G[idx]);
+          const float g = to_f(G[idx]) * gscale;
           const float mm = fmaf(beta, Mo[idx], g);
           Mo[idx] = mm;
           v = nesterov ? fmaf(beta, mm, g) : mm;
@@ -83,7 +129,7 @@ __global__ void __launch_bounds__(kNT) front_kernel(
       float v = 0.f;
       if (i < m && k < n) {
         const int64_t idx = k * m + i;
-        const float g = to_f(G[idx]);
+        const float g = to_f(G[idx]) * gscale;
         const float mm = fmaf(beta, Mo[idx], g);
         Mo[idx] = mm;
         v = nesterov ? fmaf(beta, mm, g) : mm;
@@ -127,9 +173,14 @@ __global__ void __launch_bounds__(kNT) normalize_kernel(char* ws, size_t slice_w
     v.x *= s; v.y *= s; v.z *= s; v.w *= s;
     if (in_place) {
       *reinterpret_cast<float4*>(V + i) = v;
+    } else if constexpr (sizeof(IT) == 2) {
+      uint2 u;
+      __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+      u.x = *reinterpret_cast<uint32_t*>(&a);
+      u.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(X + i) = u;
     } else {
-      X[i + 0] = from_f<IT>(v.x); X[i + 1] = from_f<IT>(v.y);
-      X[i + 2] = from_f<IT>(v.z); X[i + 3] = from_f<IT>(v.w);
+      *reinterpret_cast<float4*>(X + i) = v;
     }
   }
 }
@@ -138,12 +189,32 @@ __global__ void __launch_bounds__(kNT) normalize_kernel(char* ws, size_t slice_w
 // working layout (transposed when tr).  Optionally O is written out too.
 template <typename PT>
 __global__ void __launch_bounds__(kNT) epilogue_kernel(
-    const __grid_constant__ SlicePtrs ptrs, int64_t M, int64_t N, int64_t n_pad, int tr,
-    float decay, float lr_scale, char* ws, size_t slice_ws, size_t off_O) {
+    const __grid_constant__ SlicePtrs ptrs, int64_t M, int64_t N, int64_t n_pad, int tr, int vec,
+    float decay, float lr_scale, const int* skip, char* ws, size_t slice_ws, size_t off_O) {
+  if (skip && *skip) return;   // skipped loss-scaled step: parameters untouched
   const int s = blockIdx.y;
   const float* O = reinterpret_cast<const float*>(ws + (size_t)s * slice_ws + off_O);
   PT* W = static_cast<PT*>(ptrs.W[s]);
   float* Oout = ptrs.O[s];
+  if (!tr && vec) {
+    // 32 rows x 128 columns per block, 4 consecutive elements per thread
+    const int tiles_c4 = (int)((N + 127) / 128);
+    const int64_t r0 = (int64_t)(blockIdx.x / tiles_c4) * 32;
+    const int64_t c = (int64_t)(blockIdx.x % tiles_c4) * 128 + 4 * (threadIdx.x & 31);
+    for (int j = threadIdx.x >> 5; j < 32; j += kNT / 32) {
+      const int64_t r = r0 + j;
+      if (r < M && c < N) {
+        float o[4], w[4], wn[4];
+        load4(O + r * n_pad + c, o);
+        load4(W + r * N + c, w);
+        #pragma unroll
+        for (int e = 0; e < 4; ++e) wn[e] = fmaf(w[e], decay, -lr_scale * o[e]);
+        store4(W + r * N + c, wn);
+        if (Oout) store4(Oout + r * N + c, o);
+      }
+    }
+    return;
+  }
   __shared__ float tile[32][33];
   const int tiles_c = (int)((N + 31) / 32);
   const int64_t r0 = (int64_t)(blockIdx.x / tiles_c) * 32;
@@ -197,12 +268,22 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   const int64_t mp = g.m_pad, np = g.n_pad;
   const int nblk = (int)((mp / kFrontTileR) * (np / kFrontTileC));
   dim3 fgrid(nblk, ns);
+  // vectorised access when every row of every slice starts 16-byte aligned
+  const size_t es = g.dtype == MUON_BF16 ? 2 : 4;
+  int vec = (g.n % 4 == 0 && g.N % 4 == 0) ? 1 : 0;
+  for (int i = 0; i < ns && vec; ++i) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptrs.W[i]) | reinterpret_cast<uintptr_t>(ptrs.G[i]);
+    if (a % (4 * es) || reinterpret_cast<uintptr_t>(ptrs.Mom[i]) % 16) vec = 0;
+    if (ptrs.O[i] && reinterpret_cast<uintptr_t>(ptrs.O[i]) % 16) vec = 0;
+  }
   if (g.dtype == MUON_BF16)
-    front_kernel<__nv_bfloat16><<<fgrid, kNT, 0, s>>>(ptrs, g.m, g.n, mp, np, g.tr, st.beta,
-                                                      st.nesterov, ws, sws, off.V, off.part);
+    front_kernel<__nv_bfloat16><<<fgrid, kNT, 0, s>>>(ptrs, g.m, g.n, mp, np, g.tr, vec, st.beta,
+                                                      st.nesterov, st.gscale, st.skip, ws, sws,
+                                                      off.V, off.part);
   else
-    front_kernel<float><<<fgrid, kNT, 0, s>>>(ptrs, g.m, g.n, mp, np, g.tr, st.beta,
-                                              st.nesterov, ws, sws, off.V, off.part);
+    front_kernel<float><<<fgrid, kNT, 0, s>>>(ptrs, g.m, g.n, mp, np, g.tr, vec, st.beta,
+                                              st.nesterov, st.gscale, st.skip, ws, sws, off.V,
+                                              off.part);
   finalize_kernel<<<ns, kNT, 0, s>>>(ws, sws, off.part, off.inv, nblk, st.eps);
   const int64_t cnt = mp * np;
   int nb = (int)((cnt / 4 + kNT - 1) / kNT);
@@ -215,7 +296,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
     for (int t = 0; t < st.T; ++t) {
       const bool last = t == st.T - 1;
       TcGemm g1;
-      g1.batch = ns; g1.stride = sws; g1.err = err_word;
+      g1.batch = ns; g1.stride = sws; g1.err = err_word; g1.skip = st.skip;
       // A = X X^T (symmetric)
       g1.M = mp; g1.N = mp; g1.K = np;
       g1.A = ws + xin; g1.B = ws + xin; g1.D = ws + off.A; g1.sym = 1;
@@ -230,7 +311,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
       if (e != cudaSuccess) return e;
       // X' = B X + a*X, X as an N-major B operand; fp32 O on the last step
       TcGemm g3;
-      g3.batch = ns; g3.stride = sws; g3.err = err_word;
+      g3.batch = ns; g3.stride = sws; g3.err = err_word; g3.skip = st.skip;
       g3.M = mp; g3.N = np; g3.K = mp;
       g3.A = ws + off.B; g3.B = ws + xin; g3.C = ws + xin; g3.b_mn = 1;
       g3.alpha = 1.f; g3.beta = st.a;
@@ -271,21 +352,68 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
     if (e != cudaSuccess) return e;
     const size_t tmp = xin; xin = xout; xout = tmp;
   }
-  const int tiles = (int)(((g.M + 31) / 32) * ((g.N + 31) / 32));
+  const int tiles = (!g.tr && vec) ? (int)(((g.M + 31) / 32) * ((g.N + 127) / 128))
+                                   : (int)(((g.M + 31) / 32) * ((g.N + 31) / 32));
   const float decay = 1.f - st.lr * st.wd;
   const float lrs = st.lr * g.scale;
   if (g.dtype == MUON_BF16)
-    epilogue_kernel<__nv_bfloat16><<<dim3(tiles, ns), kNT, 0, s>>>(ptrs, g.M, g.N, np, g.tr,
-                                                                  decay, lrs, ws, sws, off.V);
+    epilogue_kernel<__nv_bfloat16><<<dim3(tiles, ns), kNT, 0, s>>>(ptrs, g.M, g.N, np, g.tr, vec,
+                                                                  decay, lrs, st.skip, ws, sws,
+                                                                  off.V);
   else
-    epilogue_kernel<float><<<dim3(tiles, ns), kNT, 0, s>>>(ptrs, g.M, g.N, np, g.tr, decay,
-                                                          lrs, ws, sws, off.V);
+    epilogue_kernel<float><<<dim3(tiles, ns), kNT, 0, s>>>(ptrs, g.M, g.N, np, g.tr, vec, decay,
+                                                          lrs, st.skip, ws, sws, off.V);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 int dense_launches(int ns_steps) { return 4 + 3 * ns_steps; }
+
+namespace {
+// *found = 1 when any value of the chunk's gradients is inf or NaN
+template <typename PT>
+__global__ void __launch_bounds__(kNT) check_finite_kernel(const __grid_constant__ SlicePtrs ptrs,
+                                                           int64_t count, int vec, int* found) {
+  const PT* G = static_cast<const PT*>(ptrs.G[blockIdx.y]);
+  int bad = 0;
+  const int64_t stride = (int64_t)gridDim.x * kNT;
+  if (vec) {
+    for (int64_t i = ((int64_t)blockIdx.x * kNT + threadIdx.x) * 4; i < count; i += stride * 4) {
+      float v[4];
+      if (i + 3 < count) {
+        load4(G + i, v);
+      } else {
+        for (int e = 0; e < 4; ++e) v[e] = i + e < count ? to_f(G[i + e]) : 0.f;
+      }
+      #pragma unroll
+      for (int e = 0; e < 4; ++e) bad |= !isfinite(v[e]);
+    }
+  } else {
+    for (int64_t i = (int64_t)blockIdx.x * kNT + threadIdx.x; i < count; i += stride)
+      bad |= !isfinite(to_f(G[i]));
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) *found = 1;
+}
+}  // namespace
+
+cudaError_t launch_check_finite(const Group& g, const SlicePtrs& ptrs, int nslices, int* found,
+                                cudaStream_t s) {
+  const int64_t count = g.M * g.N;
+  const size_t es = g.dtype == MUON_BF16 ? 2 : 4;
+  int vec = 1;
+  for (int i = 0; i < nslices && vec; ++i)
+    if (reinterpret_cast<uintptr_t>(ptrs.G[i]) % (4 * es)) vec = 0;
+  int64_t per = (count + kNT * 16 - 1) / (kNT * 16);
+  if (per > 64) per = 64;
+  if (per < 1) per = 1;
+  dim3 grid((unsigned)per, (unsigned)nslices);
+  if (g.dtype == MUON_BF16)
+    check_finite_kernel<__nv_bfloat16><<<grid, kNT, 0, s>>>(ptrs, count, vec, found);
+  else
+    check_finite_kernel<float><<<grid, kNT, 0, s>>>(ptrs, count, vec, found);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& ptrs,
                                      int nslices, const StepArgs& st, char* ws,

@@ -68,6 +68,8 @@ struct StepArgs {
   int T;
   float a, b, c;
   float eps;
+  float gscale = 1.f;          // gradients are multiplied by this (1/loss scale)
+  const int* skip = nullptr;   // device flag: when set, the step changes nothing
 };
 
 size_t dense_slice_ws(const Group& g, int mode);
@@ -81,5 +83,9 @@ cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& 
                                      int* err_word, cudaStream_t s);
 
 int dense_launches(int ns_steps);
+
+// Sets *found to 1 when any gradient value of the chunk is inf or NaN.
+cudaError_t launch_check_finite(const Group& g, const SlicePtrs& ptrs, int nslices, int* found,
+                                cudaStream_t s);
 
 }  // namespace muon

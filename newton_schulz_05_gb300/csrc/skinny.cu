@@ -74,9 +74,6 @@ __device__ __forceinline__ uint32_t pack_h(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
   return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
 }
-__device__ __forceinline__ float2 unpack_h(uint32_t u) {
-  return __half22float2(*reinterpret_cast<__half2*>(&u));
-}
 __device__ __forceinline__ uint32_t movt(uint32_t a) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
@@ -234,35 +231,39 @@ struct SkinnySmem {
   static constexpr int NP = (MB + 1) / 2;
   static constexpr int MPX = 16 * NP;
   static constexpr size_t MAT = sizeof(float) * MP * MP;
-  // ring of row stages (bulk copies): SW columns, one superchunk per warp;
-  // row pitches padded so the fragment reads of a warp hit distinct banks
-  static constexpr int SW = 32 * NW;
-  static constexpr int PITCH_G = SW * ES + (ES == 2 ? 32 : 64);
-  static constexpr int PITCH_M = SW * 4 + 64;
-  static constexpr size_t STAGE = (size_t)MP * (PITCH_G + PITCH_M);
-  static constexpr int FIT = (int)((212 * 1024) / STAGE);
-  static constexpr bool STAGED = MB <= 4 && FIT >= 2;
-  static constexpr int NSTAGE = !STAGED ? 0 : (FIT >= 4 ? 4 : FIT);
-  static constexpr size_t RING = STAGED ? NSTAGE * STAGE : 0;
-  // the warp partials and the m x m matrices reuse the ring between the two
-  // passes (NW >= 8 > 5 matrices)
-  static constexpr size_t ring = 0;
+  // for m > 32 the five m x m matrices reuse the warp-partial region, dead
+  // once the CTA partial is formed (NW = 8 >= 5); no ring is used there
+  static constexpr bool ALIAS = MB > 4;
   static constexpr size_t gram_w = 0;                       // NW warp partials
-  static constexpr size_t mat_a = 0;                        // A_t
+  static constexpr size_t mat_a = ALIAS ? 0 : gram_w + NW * MAT;   // A_t
   static constexpr size_t mat_p = mat_a + MAT;              // P_t
   static constexpr size_t mat_q = mat_p + MAT;              // Q_t = P_{t-1} ... P_0
   static constexpr size_t mat_t1 = mat_q + MAT;             // scratch products
   static constexpr size_t mat_t2 = mat_t1 + MAT;
-  static constexpr size_t region = RING > NW * MAT ? RING : NW * MAT;
-  static constexpr size_t gram_c = region;                  // CTA partial (cluster-visible)
+  static constexpr size_t gram_c = ALIAS ? gram_w + NW * MAT : mat_t2 + MAT;  // CTA partial
   static constexpr size_t qh = gram_c + MAT;                // fp16 Q, the MMA A operand
   static constexpr size_t bars = (qh + sizeof(__half) * MPX * MPX + 15) & ~size_t(15);
-  static constexpr size_t misc = bars + 8 * 8 + 8 * 4;      // 8 mbarriers, 8 counters
-  static constexpr size_t total = misc + 64 * sizeof(float) + 16;
+  static constexpr size_t misc = bars + 12 * 8 + 12 * 4;    // 12 mbarriers, 12 counters
+  static constexpr size_t ring = (misc + 64 * sizeof(float) + 16 + 127) & ~size_t(127);
+  // ring of row stages (bulk copies), SW columns = one superchunk per warp;
+  // row pitches padded so the fragment reads of a warp hit distinct banks.
+  // Pass 1 stages hold G and M rows, pass 2 stages only W rows, so the same
+  // bytes hold more pass-2 stages.
+  static constexpr int SW = 32 * NW;
+  static constexpr int PITCH_G = SW * ES + (ES == 2 ? 32 : 64);
+  static constexpr int PITCH_M = SW * 4 + 64;
+  static constexpr size_t STAGE = (size_t)MP * (PITCH_G + PITCH_M);
+  static constexpr size_t STAGE_W = (size_t)MP * PITCH_G;
+  static constexpr size_t BUDGET = 224 * 1024 > ring ? 224 * 1024 - ring : 0;
+  static constexpr int FIT = (int)(BUDGET / STAGE);
+  static constexpr bool STAGED = !ALIAS && FIT >= 2;
+  static constexpr int NSTAGE = !STAGED ? 0 : (FIT >= 4 ? 4 : FIT);
+  static constexpr size_t RING = STAGED ? NSTAGE * STAGE : 0;
+  static constexpr int NSTAGE_W = !STAGED ? 0 : ((int)(RING / STAGE_W) >= 8 ? 8 : (int)(RING / STAGE_W));
+  static constexpr size_t total = ring + RING;
   // one CTA per SM: a second CTA on the SM would wait for tensor memory
   static constexpr size_t launch = total > 120 * 1024 ? total : 120 * 1024;
-  static_assert(NW >= 5, "matrices alias the warp partials");
-  static_assert(!STAGED || NSTAGE >= 2, "ring depth");
+  static_assert(!STAGED || (NSTAGE >= 2 && NSTAGE_W >= 2), "ring depth");
   static_assert(launch <= 227 * 1024, "shared memory");
 };
 
@@ -322,7 +323,9 @@ __device__ __forceinline__ void mat_mul(float* D, const float* A, const float* B
   for (int x = 0; x < TB; ++x)
     #pragma unroll
     for (int y = 0; y < TB; ++y) acc[x][y] = 0.f;
-  #pragma unroll 4
+  // fully unrolled for the small m of this kernel: every shared-memory load
+  // of the product is issued before the dependent FMA chain runs
+  #pragma unroll
   for (int k = 0; k < MP; ++k) {
     float av[TB], bv[TB];
     #pragma unroll
@@ -363,6 +366,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   constexpr int COLS_W = 512 / (NW / 4);
   constexpr int LOOKAHEAD = 3;   // superchunks prefetched into L2 ahead of use (direct path)
   constexpr int NSTG = S::NSTAGE > 0 ? S::NSTAGE : 1;
+  constexpr int NSTW = S::NSTAGE_W > 0 ? S::NSTAGE_W : 1;
   extern __shared__ __align__(128) unsigned char smem[];
   float* gram_w = reinterpret_cast<float*>(smem + S::gram_w);
   float* gram_c = reinterpret_cast<float*>(smem + S::gram_c);
@@ -375,8 +379,10 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   float* red = reinterpret_cast<float*>(smem + S::misc);     // NW floats
   float* norm_slot = red + 32;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 48);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::bars);  // stage landed
-  int* done_cnt = reinterpret_cast<int*>(smem + S::bars + 64);     // warps done with a stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::bars);  // pass-1 stage landed
+  uint64_t* full_w = full + 4;                                      // pass-2 stage landed
+  int* done_cnt = reinterpret_cast<int*>(smem + S::bars + 96);     // warps done with a stage
+  int* done_w = done_cnt + 4;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -389,11 +395,13 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   float* Mo = p.ptrs.Mom[slice];
   float* Oout = p.ptrs.O[slice];
   const StepArgs& st = p.st;
+  // a loss-scaled step whose gradients hold an inf or NaN changes nothing
+  if (st.skip && *st.skip) return;
 
   for (int e = tid; e < MPX * MPX; e += NT) qh[e] = __float2half_rn(0.f);
   const bool staged = S::STAGED && p.staged;
   if (tid == 0) {
-    for (int b = 0; b < 8; ++b) { mbar_init(&full[b], 1); done_cnt[b] = 0; }
+    for (int b = 0; b < 12; ++b) { mbar_init(&full[b], 1); done_cnt[b] = 0; }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
@@ -418,45 +426,43 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   const int c_lo = jc0 * 32, c_hi = min(p.n, jc1 * 32);
   const int nstage = jc1 > jc0 ? (c_hi - c_lo + S::SW - 1) / S::SW : 0;   // stages per pass
   bool wait_ok = true;
-  // stage k < nstage: G and M rows of columns [c_lo + k*SW, ...);
-  // stage k >= nstage: W rows of stage k - nstage.  One thread issues it.
-  auto issue_stage = [&](int k) {
+  // Stage k of pass `w2` (0: G and M rows, 1: W rows) of columns
+  // [c_lo + k*SW, ...), issued by all lanes of one warp (lane i copies row i).
+  auto issue_stage = [&](int k, int w2) {
     if (!S::STAGED) return;
-    const int b = k % NSTG;
-    const int s2 = k < nstage ? k : k - nstage;
-    const int c0 = c_lo + s2 * S::SW;
+    const int c0 = c_lo + k * S::SW;
     const int cols = min(S::SW, c_hi - c0);
-    unsigned char* base = smem + S::ring + (size_t)b * S::STAGE;
-    if (k < nstage) {
-      mbar_expect_tx(&full[b], (uint32_t)(p.m * cols * ((int)sizeof(PT) + 4)));
-      for (int i = 0; i < p.m; ++i) {
-        bulk_load(base + i * S::PITCH_G, G + (size_t)i * p.n + c0, cols * (int)sizeof(PT), &full[b]);
-        bulk_load(base + MP * S::PITCH_G + i * S::PITCH_M, Mo + (size_t)i * p.n + c0, cols * 4, &full[b]);
-      }
-    } else {
-      mbar_expect_tx(&full[b], (uint32_t)(p.m * cols * (int)sizeof(PT)));
-      for (int i = 0; i < p.m; ++i)
-        bulk_load(base + i * S::PITCH_G, W + (size_t)i * p.n + c0, cols * (int)sizeof(PT), &full[b]);
-    }
-  };
-  // a warp is done with stage k: the last one refills its buffer with stage
-  // k + NSTAGE of the same pass
-  auto release_stage = [&](int k, int k_end) {
+    uint64_t* bar = w2 ? &full_w[k % NSTW] : &full[k % NSTG];
+    unsigned char* base = smem + S::ring + (w2 ? (size_t)(k % NSTW) * S::STAGE_W : (size_t)(k % NSTG) * S::STAGE);
+    if (lane == 0)
+      mbar_expect_tx(bar, (uint32_t)(p.m * cols * ((int)sizeof(PT) + (w2 ? 0 : 4))));
     __syncwarp();
-    if (lane == 0) {
-      const int b = k % NSTG;
-      __threadfence_block();
-      if (atomicAdd(&done_cnt[b], 1) == NW - 1) {
-        done_cnt[b] = 0;
-        if (k + NSTG < k_end) {
-          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-          issue_stage(k + NSTG);
-        }
-      }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    for (int i = lane; i < p.m; i += 32) {
+      const PT* src = w2 ? W : G;
+      bulk_load(base + i * S::PITCH_G, src + (size_t)i * p.n + c0, cols * (int)sizeof(PT), bar);
+      if (!w2)
+        bulk_load(base + MP * S::PITCH_G + i * S::PITCH_M, Mo + (size_t)i * p.n + c0, cols * 4, bar);
     }
   };
-  auto stage_wait = [&](int k) {
-    if (!mbar_wait(&full[k % NSTG], (uint32_t)((k / NSTG) & 1)) && wait_ok) {
+  // every warp calls this when done with stage k; the last one refills the
+  // buffer with stage k + depth of the same pass
+  auto release_stage = [&](int k, int w2) {
+    __syncwarp();
+    const int depth = w2 ? NSTW : NSTG;
+    int last = 0;
+    if (lane == 0) {
+      int* cnt = w2 ? &done_w[k % NSTW] : &done_cnt[k % NSTG];
+      __threadfence_block();
+      if (atomicAdd(cnt, 1) == NW - 1) { *cnt = 0; last = 1; }
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last && k + depth < nstage) issue_stage(k + depth, w2);
+  };
+  auto stage_wait = [&](int k, int w2) {
+    uint64_t* bar = w2 ? &full_w[k % NSTW] : &full[k % NSTG];
+    const uint32_t par = (uint32_t)((k / (w2 ? NSTW : NSTG)) & 1);
+    if (!mbar_wait(bar, par) && wait_ok) {
       wait_ok = false;
       atomicExch(p.err, kDevErrTimeout);
     }
@@ -471,8 +477,9 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
       asm volatile("prefetch.global.L2 [%0];\n" ::"l"(Mo + off));
     }
   };
-  if (staged && tid == 0)
-    for (int k = 0; k < min(NSTG, nstage); ++k) issue_stage(k);
+  // each initial stage is issued by its own warp (a bulk copy takes tens of
+  // cycles to issue; spreading them keeps any one warp from falling behind)
+  if (staged && warp < min(NSTG, nstage)) issue_stage(warp, 0);
   for (int q = 0; q < LOOKAHEAD; ++q) prefetch_sc(q);
 
   // ---- pass 1: momentum, V (bf16 in TMEM), sum of squares, Gram of V ----------
@@ -485,11 +492,17 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
       #pragma unroll
       for (int e = 0; e < 4; ++e) gacc[P][J][e] = 0.f;
   const int npass = staged ? nstage : nslot;
+  // staged path: rows start 16-byte aligned and columns are whole 4-groups,
+  // so a lane's accesses reduce to a row base plus a column
+  float* mo_row[MB];
+  #pragma unroll
+  for (int rb = 0; rb < MB; ++rb) mo_row[rb] = Mo + (size_t)(rb * 8 + g < p.m ? rb * 8 + g : 0) * p.n;
+  auto row_ok = [&](int rb) { return rb * 8 + g < p.m; };
   for (int q = 0; q < npass; ++q) {
     const bool has = q < nslot;       // warp has a superchunk in this stage
     float gv[MB][2][4], mv[MB][2][4];
     if (staged) {
-      stage_wait(q);
+      stage_wait(q, 0);
       const unsigned char* base = smem + S::ring + (size_t)(q % NSTG) * S::STAGE;
       #pragma unroll
       for (int rb = 0; rb < MB; ++rb)
@@ -497,7 +510,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
         for (int h = 0; h < 2; ++h) {
           const int i = rb * 8 + g;
           const int cl = warp * 32 + h * 16 + 4 * t4;   // column inside the stage
-          const bool in = has && i < p.m && sc_col(q) + h * 16 + 4 * t4 < p.n;
+          const bool in = has && row_ok(rb) && sc_col(q) + h * 16 + 4 * t4 < p.n;
           if (in) {
             if constexpr (sizeof(PT) == 2) {
               const uint2 u = *reinterpret_cast<const uint2*>(base + i * S::PITCH_G + cl * 2);
@@ -514,7 +527,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
             for (int e = 0; e < 4; ++e) gv[rb][h][e] = mv[rb][h][e] = 0.f;
           }
         }
-      release_stage(q, nstage);
+      release_stage(q, 0);
     } else {
       prefetch_sc(q + LOOKAHEAD);
       const int cb = sc_col(q);
@@ -536,12 +549,20 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
         float vv[4];
         #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float mm = fmaf(st.beta, mv[rb][h][e], gv[rb][h][e]);
+          const float gg = gv[rb][h][e] * st.gscale;
+          const float mm = fmaf(st.beta, mv[rb][h][e], gg);
           mv[rb][h][e] = mm;
-          vv[e] = st.nesterov ? fmaf(st.beta, mm, gv[rb][h][e]) : mm;
+          vv[e] = st.nesterov ? fmaf(st.beta, mm, gg) : mm;
           ss = fmaf(vv[e], vv[e], ss);
         }
-        acc_.store_f32(Mo, rb * 8 + g, cb + h * 16 + 4 * t4, mv[rb][h]);
+        if (staged) {
+          const int c = cb + h * 16 + 4 * t4;
+          if (row_ok(rb) && c < p.n)
+            *reinterpret_cast<float4*>(mo_row[rb] + c) =
+                make_float4(mv[rb][h][0], mv[rb][h][1], mv[rb][h][2], mv[rb][h][3]);
+        } else {
+          acc_.store_f32(Mo, rb * 8 + g, cb + h * 16 + 4 * t4, mv[rb][h]);
+        }
         xr[rb][2 * h] = pack_bf16(vv[0], vv[1]);
         xr[rb][2 * h + 1] = pack_bf16(vv[2], vv[3]);
       }
@@ -569,7 +590,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   }
 
   // ---- cluster-wide ||V||^2 and V V^T (fixed order: warps, then ranks) -----------
-  __syncthreads();   // the warp partials reuse the ring
+  __syncthreads();   // every pass-1 stage is consumed: the ring takes W rows
   {
     float* gw = gram_w + warp * MP * MP;
     #pragma unroll
@@ -589,6 +610,9 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red[warp] = ss;
   tm_wait_st();
+  // the parameter rows of pass 2 start streaming while the reductions and
+  // the m x m recursion run
+  if (staged && NW - 1 - warp < min(NSTW, nstage)) issue_stage(NW - 1 - warp, 1);
   __syncthreads();
   for (int e = tid; e < MP * MP; e += NT) {
     if (!gram_covered(e / MP, e % MP)) continue;
@@ -623,8 +647,15 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   for (int t = 0; t < st.T; ++t) {
     mat_mul<MP, NT, 1>(mP, mA, mA, tid, st.a, st.b, st.c);   // P = aI + bA + cA^2
     __syncthreads();
-    mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);                      // Q <- P Q
-    if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid);    // P A
+    // Q <- P Q and P A on disjoint thread sets when both fit
+    constexpr int NB2 = MatTile<MP, NT>::NB * MatTile<MP, NT>::NB;
+    if (2 * NB2 <= NT) {
+      if (tid < NB2) mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
+      else if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid - NB2);
+    } else {
+      mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
+      if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid);
+    }
     __syncthreads();
     { float* x = mQ; mQ = mT1; mT1 = x; }
     if (t + 1 < st.T) {
@@ -654,10 +685,6 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
 
   // ---- pass 2: O = Q X_0 and W' = W (1 - lr wd) - lr s O -------------------------
   // (the ring held the m x m matrices until the barrier above)
-  if (staged && tid == 0) {
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    for (int k = 0; k < min(NSTG, nstage); ++k) issue_stage(nstage + k);
-  }
   float wbuf[MB][2][4];
   auto load_w = [&](int q) {
     const int cb = sc_col(q);
@@ -677,15 +704,15 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     }
     float wcur[MB][2][4];
     if (staged) {
-      stage_wait(nstage + q);
-      const unsigned char* base = smem + S::ring + (size_t)((nstage + q) % NSTG) * S::STAGE;
+      stage_wait(q, 1);
+      const unsigned char* base = smem + S::ring + (size_t)(q % NSTW) * S::STAGE_W;
       #pragma unroll
       for (int rb = 0; rb < MB; ++rb)
         #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int i = rb * 8 + g;
           const int cl = warp * 32 + h * 16 + 4 * t4;
-          const bool in = has && i < p.m && sc_col(q) + h * 16 + 4 * t4 < p.n;
+          const bool in = has && row_ok(rb) && sc_col(q) + h * 16 + 4 * t4 < p.n;
           if (in) {
             if constexpr (sizeof(PT) == 2) {
               const uint2 u = *reinterpret_cast<const uint2*>(base + i * S::PITCH_G + cl * 2);
@@ -700,7 +727,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
             for (int e = 0; e < 4; ++e) wcur[rb][h][e] = 0.f;
           }
         }
-      release_stage(nstage + q, 2 * nstage);
+      release_stage(q, 1);
     } else {
       #pragma unroll
       for (int rb = 0; rb < MB; ++rb)
@@ -755,8 +782,24 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
         float wn[4];
         #pragma unroll
         for (int e = 0; e < 4; ++e) wn[e] = fmaf(wcur[rb][h][e], p.decay, -p.lrs * ov[e]);
-        acc_.store(W, i, c, wn);
-        if (Oout) acc_.store_f32(Oout, i, c, ov);
+        if (staged) {
+          if (row_ok(rb) && c < p.n) {
+            PT* wp = W + (mo_row[rb] - Mo) + c;     // same row offset as the momentum
+            if constexpr (sizeof(PT) == 2) {
+              uint2 u;
+              u.x = pack_bf16(wn[0], wn[1]);
+              u.y = pack_bf16(wn[2], wn[3]);
+              *reinterpret_cast<uint2*>(wp) = u;
+            } else {
+              *reinterpret_cast<float4*>(wp) = make_float4(wn[0], wn[1], wn[2], wn[3]);
+            }
+            if (Oout)
+              *reinterpret_cast<float4*>(Oout + (mo_row[rb] - Mo) + c) = make_float4(ov[0], ov[1], ov[2], ov[3]);
+          }
+        } else {
+          acc_.store(W, i, c, wn);
+          if (Oout) acc_.store_f32(Oout, i, c, ov);
+        }
       }
   }
   // no CTA may leave while a cluster peer can still read its shared memory

@@ -15,7 +15,8 @@ namespace {
 muon_status step_impl(const muon_plan_t* P, void* const* params, const void* const* grads,
                       float* const* momentum, float lr, float beta, float wd, int nesterov,
                       int ns_steps, const float* coeffs, void* workspace, size_t ws_bytes,
-                      void* stream, float* const* ortho) {
+                      void* stream, float* const* ortho, float inv_scale = 1.f,
+                      int* found_inf = nullptr) {
   if (!P) return MUON_ERR_INVALID_ARG;
   const int np = (int)P->shapes.size();
   if (np > 0 && (!params || !grads || !momentum)) return MUON_ERR_INVALID_ARG;
@@ -34,27 +35,44 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
   st.c = coeffs ? coeffs[2] : 2.0315f;
   if (!std::isfinite(st.a) || !std::isfinite(st.b) || !std::isfinite(st.c)) return MUON_ERR_INVALID_ARG;
   st.eps = P->opt.eps;
+  if (!std::isfinite(inv_scale)) return MUON_ERR_INVALID_ARG;
+  st.gscale = inv_scale;
+  st.skip = found_inf;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   int* err_word = reinterpret_cast<int*>(ws);
   char* body = ws + kHeaderBytes;
 
   SlicePtrs ptrs;
-  for (const Group& g : P->groups) {
-    const int cnt = g.count();
+  auto fill = [&](const Group& g, int c0, int ns) {
     const size_t es = g.dtype == MUON_BF16 ? 2 : 4;
     const int64_t mn = g.M * g.N;
+    for (int i = 0; i < ns; ++i) {
+      const int p = g.slice_param[c0 + i];
+      const int64_t off = g.slice_e[c0 + i] * mn;
+      ptrs.W[i] = static_cast<char*>(params[p]) + off * es;
+      ptrs.G[i] = static_cast<const char*>(grads[p]) + off * es;
+      ptrs.Mom[i] = momentum[p] + off;
+      ptrs.O[i] = ortho ? ortho[p] + off : nullptr;
+    }
+  };
+  if (found_inf) {
+    // loss-scaled step: every gradient value is checked before any state
+    // changes; the kernels below return at once when the flag is set
+    if (cudaMemsetAsync(found_inf, 0, sizeof(int), s) != cudaSuccess) return MUON_ERR_CUDA;
+    for (const Group& g : P->groups)
+      for (int c0 = 0; c0 < g.count(); c0 += kMaxSlicesPerLaunch) {
+        const int ns = g.count() - c0 < kMaxSlicesPerLaunch ? g.count() - c0 : kMaxSlicesPerLaunch;
+        fill(g, c0, ns);
+        if (launch_check_finite(g, ptrs, ns, found_inf, s) != cudaSuccess) return MUON_ERR_CUDA;
+      }
+  }
+  for (const Group& g : P->groups) {
+    const int cnt = g.count();
     const int per = g.kernel == MUON_KERNEL_SKINNY ? kMaxSlicesPerLaunch : g.chunk;
     for (int c0 = 0; c0 < cnt; c0 += per) {
       const int ns = cnt - c0 < per ? cnt - c0 : per;
-      for (int i = 0; i < ns; ++i) {
-        const int p = g.slice_param[c0 + i];
-        const int64_t off = g.slice_e[c0 + i] * mn;
-        ptrs.W[i] = static_cast<char*>(params[p]) + off * es;
-        ptrs.G[i] = static_cast<const char*>(grads[p]) + off * es;
-        ptrs.Mom[i] = momentum[p] + off;
-        ptrs.O[i] = ortho ? ortho[p] + off : nullptr;
-      }
+      fill(g, c0, ns);
       cudaError_t e;
       if (g.kernel == MUON_KERNEL_SKINNY)
         e = launch_skinny(g, ptrs, ns, st, err_word, s);
@@ -86,6 +104,15 @@ muon_status muon_step_ortho(const muon_plan_t* P, void* const* params,
   if (!ortho) return MUON_ERR_INVALID_ARG;
   return step_impl(P, params, grads, momentum, lr, beta, wd, nesterov, ns_steps, coeffs,
                    workspace, ws_bytes, stream, ortho);
+}
+
+muon_status muon_step_amp(const muon_plan_t* P, void* const* params, const void* const* grads,
+                          float* const* momentum, float lr, float beta, float wd, int nesterov,
+                          int ns_steps, const float* coeffs, float inv_scale, int* found_inf,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  if (!found_inf) return MUON_ERR_INVALID_ARG;
+  return step_impl(P, params, grads, momentum, lr, beta, wd, nesterov, ns_steps, coeffs,
+                   workspace, ws_bytes, stream, nullptr, inv_scale, found_inf);
 }
 
 muon_status muon_workspace_error(const void* workspace, void* stream, int clear, int* code) {

@@ -48,6 +48,7 @@ struct TcParams {
   int b_mn;
   uint32_t idesc;
   int* err;
+  const int* skip;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -155,6 +156,7 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& b, in
 __global__ void __launch_bounds__(NTHREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ TcParams p) {
+  if (p.skip && *p.skip) return;   // skipped loss-scaled step
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -407,6 +409,7 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
   p.sym = g.sym; p.b_mn = g.b_mn;
   p.idesc = tc_idesc_f16(BM, BN, g.b_mn);
   p.err = g.err;
+  p.skip = g.skip;
   const size_t smem = tc_gemm_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);

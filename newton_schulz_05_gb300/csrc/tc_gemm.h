@@ -30,6 +30,7 @@ struct TcGemm {
   int sym = 0;
   int b_mn = 0;
   int* err = nullptr;   // device error word (bounded waits)
+  const int* skip = nullptr;  // device flag: when set, the kernel returns at once
 };
 
 cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s);

@@ -75,6 +75,9 @@ def lib():
                                         ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                         ctypes.c_int, ctypes.c_int, _dp, ctypes.c_double,
                                         ctypes.c_double, ctypes.c_int, _dp, _dp, _dp]
+        L.oracle_all_finite.restype = ctypes.c_int
+        L.oracle_all_finite.argtypes = [ctypes.c_int64, _dp]
+        L.oracle_unscale.argtypes = [ctypes.c_int64, _dp, ctypes.c_double, _dp]
         PP = ctypes.POINTER(_dp)
         L.oracle_muon_slices.restype = ctypes.c_int
         L.oracle_muon_slices.argtypes = [ctypes.c_int, _i64p, _i64p, PP, PP, PP,
@@ -197,6 +200,28 @@ def muon_slices(Ws: List, Gs: List, Moms: List, lr, beta, wd, nesterov, T=5,
         threads, PA(*[_ptr(x) for x in wo]), PA(*[_ptr(x) for x in mo]),
         PA(*[_ptr(x) for x in oo]) if want_O else None)
     return wo, mo, oo, used
+
+
+def all_finite(Gs) -> bool:
+    """True when every value of every gradient is finite (loss-scaler check)."""
+    return all(lib().oracle_all_finite(g.size, _ptr(g)) == 1 for g in (_f64(x) for x in Gs))
+
+
+def unscale(G, inv_scale: float):
+    g = _f64(G); out = np.empty_like(g)
+    lib().oracle_unscale(g.size, _ptr(g), inv_scale, _ptr(out))
+    return out
+
+
+def muon_slices_amp(Ws, Gs, Moms, lr, beta, wd, nesterov, inv_scale: float, **kw):
+    """The loss-scaled step: if any gradient value of any slice is inf or NaN
+    the step is skipped (found_inf = True, every W and M unchanged);
+    otherwise the step runs on G * inv_scale.  Returns (W's, M's, Os, found_inf)."""
+    if not all_finite(Gs):
+        return [_f64(w) for w in Ws], [_f64(m) for m in Moms], None, True
+    wo, mo, oo, _ = muon_slices(Ws, [unscale(g, inv_scale) for g in Gs], Moms, lr, beta, wd,
+                                nesterov, **kw)
+    return wo, mo, oo, False
 
 
 def param_slices(t) -> List:

@@ -236,4 +236,19 @@ int oracle_muon_slices(int nslices, const int64_t* Ms, const int64_t* Ns,
   return nt;
 }
 
+// Loss scaling (Paddle PR "Support Muon sharding optimizer comm overlap",
+// review of the AMP GradScaler path: the Muon step runs on gradients that a
+// loss scaler has multiplied by S and must unscale and check first).
+// 1 when every one of `count` values is finite, else 0.
+int oracle_all_finite(int64_t count, const double* G) {
+  for (int64_t i = 0; i < count; ++i)
+    if (!std::isfinite(G[i])) return 0;
+  return 1;
+}
+
+// Unscaled gradient: out = G * inv_scale.
+void oracle_unscale(int64_t count, const double* G, double inv_scale, double* out) {
+  for (int64_t i = 0; i < count; ++i) out[i] = G[i] * inv_scale;
+}
+
 }  // extern "C"

@@ -160,3 +160,17 @@ def test_workspace_cap_chunks_dense_groups(muon):
     assert capped.groups()[0]["chunk"] == 2
     assert capped.workspace_bytes == 256 + 2 * per
     assert capped.launches(5) == 2 * full.launches(5)
+
+
+def test_amp_step_rejects_bad_arguments(muon):
+    import torch
+    plan = muon.Plan([((24, 64), torch.bfloat16)])
+    L = muon.load()
+    P = ctypes.c_void_p * 1
+    fake = P(ctypes.c_void_p(0x1000))
+    c = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    # null found_inf, non-finite inv_scale
+    assert L.muon_step_amp(plan.handle, fake, fake, fake, 0.02, 0.95, 0.1, 1, 5, c, 1.0, None,
+                           ctypes.c_void_p(0x1000), 4096, None) == -1
+    assert L.muon_step_amp(plan.handle, fake, fake, fake, 0.02, 0.95, 0.1, 1, 5, c, float("inf"),
+                           ctypes.c_void_p(0x2000), ctypes.c_void_p(0x1000), 4096, None) == -1

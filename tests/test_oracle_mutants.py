@@ -41,6 +41,9 @@ MUTANTS = {
                            "group_N[k] == N"),
     "plan_scale_inverted": ("double ratio = (double)M / (double)N;",
                             "double ratio = (double)N / (double)M;"),
+    "finite_check_misses_nan": ("if (!std::isfinite(G[i])) return 0;",
+                                "if (std::isinf(G[i])) return 0;"),
+    "unscale_divides": ("out[i] = G[i] * inv_scale;", "out[i] = G[i] / inv_scale;"),
 }
 
 

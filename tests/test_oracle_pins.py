@@ -285,3 +285,27 @@ def test_plan_golden(fixture):
     sg, si, groups = _check_plan(shapes, [g["dtype"]] * len(shapes))
     got = [[gr["M"], gr["N"], gr["count"], int(gr["tr"])] for gr in groups]
     assert got == g["groups"]
+
+
+# ---------------------------------------------------------------- loss scaling
+def test_all_finite_matches_numpy():
+    rng = np.random.default_rng(19)
+    G = rng.standard_normal((7, 9))
+    assert oracle.all_finite([G, G])
+    for bad in (np.inf, -np.inf, np.nan):
+        H = G.copy(); H[3, 4] = bad
+        assert not oracle.all_finite([G, H]) and not np.isfinite(H).all()
+
+
+def test_unscale_by_power_of_two_is_exact_and_skips_on_inf():
+    rng = np.random.default_rng(20)
+    W = rng.standard_normal((6, 11)); G = rng.standard_normal((6, 11)); M = rng.standard_normal((6, 11))
+    S = 2.0 ** 12
+    wo, mo, oo, found = oracle.muon_slices_amp([W], [G * S], [M], 0.02, 0.95, 0.1, True, 1 / S)
+    w1, m1, o1 = oracle.muon_slice(W, G, M, 0.02, 0.95, 0.1, True)
+    assert not found
+    assert np.array_equal(wo[0], w1) and np.array_equal(mo[0], m1) and np.array_equal(oo[0], o1)
+    H = G.copy(); H[0, 0] = np.nan
+    wo, mo, oo, found = oracle.muon_slices_amp([W, W], [G, H], [M, M], 0.02, 0.95, 0.1, True, 1 / S)
+    assert found and oo is None
+    assert all(np.array_equal(x, W) for x in wo) and all(np.array_equal(x, M) for x in mo)
