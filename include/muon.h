@@ -175,6 +175,25 @@ MUON_API muon_status muon_step_amp(const muon_plan_t* plan, void* const* params,
                                    void* stream);
 
 /*
+ * AdamW for the parameters Muon does not orthogonalise (1-D biases and norm
+ * scales, or any tensor the caller keeps off the Muon path; the Paddle Muon
+ * sharding PR keeps separate 2-D and 1-D gradient buffers because the two
+ * kinds take different update rules).  Standard AdamW, bias-corrected, with
+ * decoupled weight decay, step t >= 1:
+ *   m' = b1*m + (1-b1)*g;  v' = b2*v + (1-b2)*g^2
+ *   W' = W*(1 - lr*wd) - lr * (m'/(1-b1^t)) / (sqrt(v'/(1-b2^t)) + eps)
+ *   n tensors, each contiguous with numel[i] elements (any shape): params[i]
+ *   and grads[i] of `dtype`, exp_avg[i] and exp_avg_sq[i] fp32 (updated in
+ *   place).  All device pointers; one launch per 256 tensors.
+ * Returns MUON_ERR_INVALID_ARG for null pointers, t < 1, betas outside [0,1),
+ * negative eps or non-finite hyper-parameters.
+ */
+MUON_API muon_status muon_adamw_step(int n, void* const* params, const void* const* grads,
+                                     float* const* exp_avg, float* const* exp_avg_sq,
+                                     const int64_t* numel, int dtype, float lr, float beta1,
+                                     float beta2, float eps, float wd, int step, void* stream);
+
+/*
  * Read the device error word of a workspace after synchronising `stream`.
  * *code receives MUON_OK or the first device-side error recorded
  * (MUON_ERR_DEVICE_TIMEOUT); when clear != 0 the word is reset to zero.

@@ -58,7 +58,7 @@ EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
            "muon_plan_num_groups", "muon_plan_num_slices", "muon_plan_group",
            "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
            "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static",
-           "muon_step_amp"]
+           "muon_step_amp", "muon_adamw_step"]
 
 STATIC_WORKSPACE_BYTES = 32 << 20   # MUON_STATIC_WORKSPACE_BYTES in include/muon.h
 
@@ -91,6 +91,9 @@ def load(path: str = LIB_PATH):
     L.muon_step_ortho.argtypes = step_args + [PP]
     L.muon_step_static.argtypes = step_args[:10] + [vp]
     L.muon_step_amp.argtypes = step_args[:10] + [ctypes.c_float, vp, vp, sz, vp]
+    L.muon_adamw_step.argtypes = [ctypes.c_int, PP, PP, PP, PP, ctypes.POINTER(ctypes.c_int64),
+                                  ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                  ctypes.c_float, ctypes.c_float, ctypes.c_int, vp]
     L.muon_workspace_error.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.muon_plan_launches.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.muon_plan_destroy.argtypes = [vp]
@@ -100,7 +103,7 @@ def load(path: str = LIB_PATH):
     for fn in ("muon_plan", "muon_plan_workspace_bytes", "muon_plan_num_groups",
                "muon_plan_num_slices", "muon_plan_group", "muon_plan_slice", "muon_step",
                "muon_step_ortho", "muon_workspace_error", "muon_plan_launches",
-               "muon_step_static", "muon_step_amp"):
+               "muon_step_static", "muon_step_amp", "muon_adamw_step"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -269,6 +272,32 @@ def step_amp(plan: Plan, params, grads, momentum, *, lr: float, beta: float, wd:
                                 ctypes.c_void_p(workspace.data_ptr()),
                                 workspace.numel() * workspace.element_size(),
                                 ctypes.c_void_p(_stream_handle(stream))), "muon_step_amp")
+
+
+def adamw_step(params, grads, exp_avg, exp_avg_sq, *, lr: float, beta1: float = 0.9,
+               beta2: float = 0.999, eps: float = 1e-8, wd: float = 0.0, step: int,
+               stream=None) -> None:
+    """muon_adamw_step: one AdamW step over every tensor (one launch per 256
+    tensors).  params/grads: contiguous CUDA tensors of one dtype (bf16 or
+    fp32); exp_avg/exp_avg_sq: fp32 tensors of the same sizes."""
+    n = len(params)
+    if not (len(grads) == len(exp_avg) == len(exp_avg_sq) == n):
+        raise ValueError("expected equally many params, grads and moment tensors")
+    dt = {torch.bfloat16: MUON_BF16, torch.float32: MUON_F32}.get(params[0].dtype if n else torch.float32)
+    if dt is None:
+        raise TypeError("parameters must be bf16 or fp32")
+    for p, g, m, v in zip(params, grads, exp_avg, exp_avg_sq):
+        if p.dtype != params[0].dtype or g.dtype != p.dtype or m.dtype != torch.float32 or \
+                v.dtype != torch.float32:
+            raise TypeError("dtype mismatch")
+        if not (p.numel() == g.numel() == m.numel() == v.numel()):
+            raise ValueError("size mismatch")
+        if not all(t.is_cuda and t.is_contiguous() for t in (p, g, m, v)):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    numel = (ctypes.c_int64 * max(n, 1))(*[p.numel() for p in params])
+    _check(load().muon_adamw_step(n, _ptrs(params), _ptrs(grads), _ptrs(exp_avg), _ptrs(exp_avg_sq),
+                                  numel, dt, lr, beta1, beta2, eps, wd, step,
+                                  ctypes.c_void_p(_stream_handle(stream))), "muon_adamw_step")
 
 
 def workspace_error(workspace: torch.Tensor, stream=None, clear: bool = True) -> int:

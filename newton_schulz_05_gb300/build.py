@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmuon.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["plan.cpp", "step.cu", "dense.cu", "skinny.cu", "tc_gemm.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "step.cu", "dense.cu", "skinny.cu", "tc_gemm.cu", "noalloc.cu", "adamw.cu"]
 
 
 def _nvcc() -> str:

@@ -426,19 +426,23 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   const int c_lo = jc0 * 32, c_hi = min(p.n, jc1 * 32);
   const int nstage = jc1 > jc0 ? (c_hi - c_lo + S::SW - 1) / S::SW : 0;   // stages per pass
   bool wait_ok = true;
-  // Stage k of pass `w2` (0: G and M rows, 1: W rows) of columns
-  // [c_lo + k*SW, ...), issued by all lanes of one warp (lane i copies row i).
-  auto issue_stage = [&](int k, int w2) {
+  // Rows [part*R, (part+1)*R) of stage k of pass `w2` (0: G and M rows,
+  // 1: W rows), columns [c_lo + k*SW, ...); one warp issues them, one row per
+  // lane.  Part 0 posts the stage's byte count (copies of other parts may
+  // land first: the phase cannot complete before that arrive).
+  auto issue_stage = [&](int k, int w2, int part = 0, int nparts = 1) {
     if (!S::STAGED) return;
     const int c0 = c_lo + k * S::SW;
     const int cols = min(S::SW, c_hi - c0);
     uint64_t* bar = w2 ? &full_w[k % NSTW] : &full[k % NSTG];
     unsigned char* base = smem + S::ring + (w2 ? (size_t)(k % NSTW) * S::STAGE_W : (size_t)(k % NSTG) * S::STAGE);
-    if (lane == 0)
+    if (part == 0 && lane == 0)
       mbar_expect_tx(bar, (uint32_t)(p.m * cols * ((int)sizeof(PT) + (w2 ? 0 : 4))));
     __syncwarp();
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    for (int i = lane; i < p.m; i += 32) {
+    const int R = (p.m + nparts - 1) / nparts;
+    const int r1 = min(p.m, (part + 1) * R);
+    for (int i = part * R + lane; i < r1; i += 32) {
       const PT* src = w2 ? W : G;
       bulk_load(base + i * S::PITCH_G, src + (size_t)i * p.n + c0, cols * (int)sizeof(PT), bar);
       if (!w2)
@@ -477,9 +481,12 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
       asm volatile("prefetch.global.L2 [%0];\n" ::"l"(Mo + off));
     }
   };
-  // each initial stage is issued by its own warp (a bulk copy takes tens of
-  // cycles to issue; spreading them keeps any one warp from falling behind)
-  if (staged && warp < min(NSTG, nstage)) issue_stage(warp, 0);
+  // the initial stages are issued by all warps, a few rows each (a bulk copy
+  // takes tens of cycles to issue; spread out, no warp falls behind)
+  if (staged) {
+    const int ns0 = min(NSTG, nstage), parts = NW / NSTG;
+    if (warp / parts < ns0) issue_stage(warp / parts, 0, warp % parts, parts);
+  }
   for (int q = 0; q < LOOKAHEAD; ++q) prefetch_sc(q);
 
   // ---- pass 1: momentum, V (bf16 in TMEM), sum of squares, Gram of V ----------
@@ -612,7 +619,10 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   tm_wait_st();
   // the parameter rows of pass 2 start streaming while the reductions and
   // the m x m recursion run
-  if (staged && NW - 1 - warp < min(NSTW, nstage)) issue_stage(NW - 1 - warp, 1);
+  if (staged) {
+    const int ns0 = min(NSTW, nstage), parts = NW / NSTW;
+    if (warp / parts < ns0) issue_stage(warp / parts, 1, warp % parts, parts);
+  }
   __syncthreads();
   for (int e = tid; e < MP * MP; e += NT) {
     if (!gram_covered(e / MP, e % MP)) continue;
@@ -644,30 +654,36 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   __syncthreads();
 
   // ---- m x m recursion: P_t = aI + bA_t + cA_t^2;  Q <- P_t Q;  A <- P_t A_t P_t ----
-  for (int t = 0; t < st.T; ++t) {
-    mat_mul<MP, NT, 1>(mP, mA, mA, tid, st.a, st.b, st.c);   // P = aI + bA + cA^2
-    __syncthreads();
-    // Q <- P Q and P A on disjoint thread sets when both fit
-    constexpr int NB2 = MatTile<MP, NT>::NB * MatTile<MP, NT>::NB;
-    if (2 * NB2 <= NT) {
-      if (tid < NB2) mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
-      else if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid - NB2);
-    } else {
-      mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
-      if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid);
+  // Only the warps that hold product tiles take part; they meet at a named
+  // barrier, the other warps wait at the block barrier below.
+  constexpr int NB2 = MatTile<MP, NT>::NB * MatTile<MP, NT>::NB;
+  constexpr bool PAIR = 2 * NB2 <= NT;                 // P Q and P A side by side
+  constexpr int RW = ((PAIR ? 2 * NB2 : NB2) + 31) / 32;
+  auto rsync = [&]() { asm volatile("bar.sync 1, %0;\n" ::"n"(RW * 32) : "memory"); };
+  if (warp < RW) {
+    for (int t = 0; t < st.T; ++t) {
+      mat_mul<MP, NT, 1>(mP, mA, mA, tid, st.a, st.b, st.c);   // P = aI + bA + cA^2
+      rsync();
+      if (PAIR) {
+        if (tid < NB2) mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
+        else if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid - NB2);
+      } else {
+        mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
+        if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid);
+      }
+      rsync();
+      { float* x = mQ; mQ = mT1; mT1 = x; }
+      if (t + 1 < st.T) {
+        mat_mul<MP, NT, 0>(mA, mT2, mP, tid);                  // A <- (P A) P
+        rsync();
+      }
     }
-    __syncthreads();
-    { float* x = mQ; mQ = mT1; mT1 = x; }
-    if (t + 1 < st.T) {
-      mat_mul<MP, NT, 0>(mA, mT2, mP, tid);                    // A <- (P A) P
-      __syncthreads();
+    // O = Q X_0 = (Q * inv / sp) (V * sp); the fp16 operand is the scaled Q
+    const float qscale = tot > 0.f ? inv / sp : 0.f;
+    for (int e = tid; e < MP * MP; e += RW * 32) {
+      const int i = e / MP, j = e % MP;
+      qh[i * MPX + j] = __float2half_rn(mQ[e] * qscale);
     }
-  }
-  // O = Q X_0 = (Q * inv / sp) (V * sp); the fp16 operand is the scaled Q
-  const float qscale = tot > 0.f ? inv / sp : 0.f;
-  for (int e = tid; e < MP * MP; e += NT) {
-    const int i = e / MP, j = e % MP;
-    qh[i * MPX + j] = __float2half_rn(mQ[e] * qscale);
   }
   __syncthreads();
   uint32_t afr[NP][NP][4];
@@ -695,13 +711,14 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
         acc_.template load<false>(W, rb * 8 + g, cb + h * 16 + 4 * t4, wbuf[rb][h]);
   };
   if (!staged && nslot > 0) load_w(0);
+  // V of the next superchunk is read from tensor memory one iteration ahead
+  uint32_t xn[MB][4];
+  if (nslot > 0) {
+    #pragma unroll
+    for (int rb = 0; rb < MB; ++rb) tm_ld4(taddr_w + 4 * rb, xn[rb]);
+  }
   for (int q = 0; q < npass; ++q) {
     const bool has = q < nslot;
-    uint32_t xr[MB][4];
-    if (has) {
-      #pragma unroll
-      for (int rb = 0; rb < MB; ++rb) tm_ld4(taddr_w + q * 4 * MB + 4 * rb, xr[rb]);
-    }
     float wcur[MB][2][4];
     if (staged) {
       stage_wait(q, 1);
@@ -739,6 +756,15 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     }
     if (!has) continue;
     tm_wait_ld();
+    uint32_t xr[MB][4];
+    #pragma unroll
+    for (int rb = 0; rb < MB; ++rb)
+      #pragma unroll
+      for (int r = 0; r < 4; ++r) xr[rb][r] = xn[rb][r];
+    if (q + 1 < nslot) {
+      #pragma unroll
+      for (int rb = 0; rb < MB; ++rb) tm_ld4(taddr_w + (q + 1) * 4 * MB + 4 * rb, xn[rb]);
+    }
     #pragma unroll
     for (int rb = 0; rb < MB; ++rb)
       #pragma unroll

@@ -78,6 +78,9 @@ def lib():
         L.oracle_all_finite.restype = ctypes.c_int
         L.oracle_all_finite.argtypes = [ctypes.c_int64, _dp]
         L.oracle_unscale.argtypes = [ctypes.c_int64, _dp, ctypes.c_double, _dp]
+        L.oracle_adamw.argtypes = [ctypes.c_int64, _dp, _dp, _dp, _dp, ctypes.c_double,
+                                   ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                   ctypes.c_double, ctypes.c_int, _dp, _dp, _dp]
         PP = ctypes.POINTER(_dp)
         L.oracle_muon_slices.restype = ctypes.c_int
         L.oracle_muon_slices.argtypes = [ctypes.c_int, _i64p, _i64p, PP, PP, PP,
@@ -222,6 +225,16 @@ def muon_slices_amp(Ws, Gs, Moms, lr, beta, wd, nesterov, inv_scale: float, **kw
     wo, mo, oo, _ = muon_slices(Ws, [unscale(g, inv_scale) for g in Gs], Moms, lr, beta, wd,
                                 nesterov, **kw)
     return wo, mo, oo, False
+
+
+def adamw(W, G, M, V, lr, beta1, beta2, eps, wd, step: int):
+    """AdamW step (bias-corrected, decoupled decay) for one tensor of any
+    shape.  Returns (W', M', V') in fp64."""
+    w = _f64(W); g = _f64(G); m = _f64(M); v = _f64(V)
+    wo = np.empty_like(w); mo = np.empty_like(w); vo = np.empty_like(w)
+    lib().oracle_adamw(w.size, _ptr(w), _ptr(g), _ptr(m), _ptr(v), lr, beta1, beta2, eps, wd,
+                       step, _ptr(wo), _ptr(mo), _ptr(vo))
+    return wo, mo, vo
 
 
 def param_slices(t) -> List:

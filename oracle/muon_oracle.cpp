@@ -251,4 +251,23 @@ void oracle_unscale(int64_t count, const double* G, double inv_scale, double* ou
   for (int64_t i = 0; i < count; ++i) out[i] = G[i] * inv_scale;
 }
 
+// AdamW for the parameters Muon does not orthogonalise (1-D and other
+// non-matrix tensors; the Paddle Muon sharding PR keeps separate 2-D and 1-D
+// communication buffers because the two kinds take different update rules).
+// Standard AdamW with bias correction and decoupled weight decay, step t >= 1:
+//   m' = b1*m + (1-b1)*g;  v' = b2*v + (1-b2)*g^2
+//   W' = W*(1 - lr*wd) - lr * (m'/(1-b1^t)) / (sqrt(v'/(1-b2^t)) + eps)
+void oracle_adamw(int64_t count, const double* W, const double* G, const double* Mm,
+                  const double* Vv, double lr, double b1, double b2, double eps, double wd,
+                  int t, double* W_out, double* M_out, double* V_out) {
+  const double c1 = 1.0 - std::pow(b1, t), c2 = 1.0 - std::pow(b2, t);
+  for (int64_t i = 0; i < count; ++i) {
+    const double m = b1 * Mm[i] + (1.0 - b1) * G[i];
+    const double v = b2 * Vv[i] + (1.0 - b2) * G[i] * G[i];
+    M_out[i] = m;
+    V_out[i] = v;
+    W_out[i] = W[i] * (1.0 - lr * wd) - lr * (m / c1) / (std::sqrt(v / c2) + eps);
+  }
+}
+
 }  // extern "C"

@@ -1,0 +1,79 @@
+"""muon_adamw_step: AdamW for the parameters Muon does not orthogonalise
+(1-D biases and norm scales, and any other tensor kept off the Muon path),
+one launch for many tensors, against the fp64 oracle element by element.
+
+Tolerances: moments within 1e-6 relative (fp32 storage of fp64 math);
+parameters within one ulp of the oracle's W' (bf16 round-to-nearest-even)
+plus 4 * 2^-24 of |W (1 - lr wd)| + lr |update| (fp32 intermediates, which
+matter where the two terms cancel), for fp32 parameters the same bound in
+fp32 ulps.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import bf16_ulp, muon
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.1)
+SIZES = [1, 3, 24, 1000, 4096, 4097, 10240, 70001, 2 * 4096 * 3 + 5]
+
+
+def _run(dtype, steps=3, sizes=SIZES):
+    m = muon()
+    W = [synth.draw((n,), 0.02, synth.param_seed(1, i), dtype) for i, n in enumerate(sizes)]
+    Gs = [[synth.draw((n,), 1e-2, synth.param_seed(10 + t, i), dtype) for i, n in enumerate(sizes)]
+          for t in range(steps)]
+    Wd = [w.cuda() for w in W]
+    Md = [torch.zeros(n, device="cuda") for n in sizes]
+    Vd = [torch.zeros(n, device="cuda") for n in sizes]
+    Wr = [w.double().numpy() for w in W]
+    Mr = [np.zeros(n) for n in sizes]
+    Vr = [np.zeros(n) for n in sizes]
+    for t in range(1, steps + 1):
+        G = Gs[t - 1]
+        W0 = [w.cpu() for w in Wd]
+        m.adamw_step(Wd, [g.cuda() for g in G], Md, Vd, step=t, **HP)
+        torch.cuda.synchronize()
+        for i in range(len(sizes)):
+            # teacher-forced: the oracle starts from the GPU's state of step t-1
+            wo, mo, vo = oracle.adamw(W0[i], G[i], Mr[i], Vr[i], HP["lr"], HP["beta1"],
+                                      HP["beta2"], HP["eps"], HP["wd"], t)
+            mg = Md[i].double().cpu().numpy(); vg = Vd[i].double().cpu().numpy()
+            assert np.all(np.abs(mg - mo) <= 1e-6 * np.abs(mo) + 1e-30), (t, i)
+            assert np.all(np.abs(vg - vo) <= 1e-6 * np.abs(vo) + 1e-38), (t, i)
+            wg = Wd[i].double().cpu().numpy()
+            w0 = W0[i].double().numpy()
+            upd = np.abs(wo - w0 * (1 - HP["lr"] * HP["wd"]))
+            slack = 4 * 2.0 ** -24 * (np.abs(w0) + upd)
+            if dtype == torch.bfloat16:
+                wr = torch.from_numpy(wo).to(torch.bfloat16).double().numpy()
+                ulp = np.maximum(bf16_ulp(wr), bf16_ulp(wg))
+            else:
+                wr = wo
+                ulp = np.spacing(np.abs(wo).astype(np.float32)).astype(np.float64)
+            assert np.all(np.abs(wg - wr) <= ulp + slack), (t, i)
+            Mr[i], Vr[i] = mg, vg
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_adamw_matches_oracle(dtype):
+    _run(dtype)
+
+
+def test_adamw_many_tensors_in_several_launches():
+    # more than 256 tensors: the launch is split, results are unchanged
+    _run(torch.bfloat16, steps=1, sizes=[(i % 7) * 97 + 1 for i in range(300)])
+
+
+def test_adamw_zero_lr_keeps_params():
+    m = muon()
+    W = [torch.randn(n, device="cuda").bfloat16() for n in (5, 1000)]
+    W0 = [w.clone() for w in W]
+    m.adamw_step(W, [torch.randn_like(w) for w in W], [torch.zeros(w.numel(), device="cuda") for w in W],
+                 [torch.zeros(w.numel(), device="cuda") for w in W], lr=0.0, wd=0.1, step=1)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(W, W0))

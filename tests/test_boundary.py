@@ -174,3 +174,17 @@ def test_amp_step_rejects_bad_arguments(muon):
                            ctypes.c_void_p(0x1000), 4096, None) == -1
     assert L.muon_step_amp(plan.handle, fake, fake, fake, 0.02, 0.95, 0.1, 1, 5, c, float("inf"),
                            ctypes.c_void_p(0x2000), ctypes.c_void_p(0x1000), 4096, None) == -1
+
+
+def test_adamw_rejects_bad_arguments(muon):
+    L = muon.load()
+    P = ctypes.c_void_p * 1
+    fake = P(ctypes.c_void_p(0x1000))
+    n = (ctypes.c_int64 * 1)(10)
+    args = lambda **kw: [kw.get("n", 1), fake, fake, fake, fake, n, kw.get("dt", 0), 1e-3,
+                         kw.get("b1", 0.9), 0.999, 1e-8, 0.0, kw.get("t", 1), None]
+    assert L.muon_adamw_step(*args(t=0)) == -1
+    assert L.muon_adamw_step(*args(b1=1.0)) == -1
+    assert L.muon_adamw_step(*args(dt=5)) == -3
+    assert L.muon_adamw_step(*args(n=-1)) == -1
+    assert L.muon_adamw_step(0, None, None, None, None, None, 0, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, None) == 0

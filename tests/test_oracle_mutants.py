@@ -44,6 +44,11 @@ MUTANTS = {
     "finite_check_misses_nan": ("if (!std::isfinite(G[i])) return 0;",
                                 "if (std::isinf(G[i])) return 0;"),
     "unscale_divides": ("out[i] = G[i] * inv_scale;", "out[i] = G[i] / inv_scale;"),
+    "adamw_no_bias_correction": ("const double c1 = 1.0 - std::pow(b1, t), c2 = 1.0 - std::pow(b2, t);",
+                                 "const double c1 = 1.0, c2 = 1.0 - std::pow(b2, t);"),
+    "adamw_eps_inside_sqrt": ("(std::sqrt(v / c2) + eps)", "std::sqrt(v / c2 + eps)"),
+    "adamw_coupled_decay": ("W_out[i] = W[i] * (1.0 - lr * wd) - lr * (m / c1)",
+                            "W_out[i] = W[i] - lr * (m / c1 + wd * W[i])"),
 }
 
 

@@ -309,3 +309,40 @@ def test_unscale_by_power_of_two_is_exact_and_skips_on_inf():
     wo, mo, oo, found = oracle.muon_slices_amp([W, W], [G, H], [M, M], 0.02, 0.95, 0.1, True, 1 / S)
     assert found and oo is None
     assert all(np.array_equal(x, W) for x in wo) and all(np.array_equal(x, M) for x in mo)
+
+
+# ---------------------------------------------------------------- AdamW (non-matrix parameters)
+def test_adamw_first_step_closed_form():
+    # from zero state the bias-corrected moments are g and g^2: the step is
+    # lr * g / (|g| + eps) plus the decoupled decay
+    rng = np.random.default_rng(22)
+    W = rng.standard_normal(301); G = rng.standard_normal(301) * 1e-3
+    Z = np.zeros_like(W)
+    wo, mo, vo = oracle.adamw(W, G, Z, Z, 1e-3, 0.9, 0.999, 1e-8, 0.1, 1)
+    np.testing.assert_allclose(mo, 0.1 * G, rtol=1e-15, atol=0)
+    np.testing.assert_allclose(vo, 0.001 * G * G, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(wo, W * (1 - 1e-4) - 1e-3 * G / (np.abs(G) + 1e-8), rtol=1e-12, atol=1e-15)
+
+
+def test_adamw_constant_gradient_keeps_the_first_step():
+    # constant g: m_t = g(1-b1^t), v_t = g^2(1-b2^t), so every bias-corrected
+    # step equals the first one
+    rng = np.random.default_rng(23)
+    G = rng.standard_normal(64)
+    W = np.zeros(64); M = np.zeros(64); V = np.zeros(64)
+    for t in range(1, 8):
+        Wn, M, V = oracle.adamw(W, G, M, V, 1e-2, 0.9, 0.99, 1e-12, 0.0, t)
+        np.testing.assert_allclose(Wn - W, -1e-2 * np.sign(G), rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(M, G * (1 - 0.9 ** t), rtol=1e-12, atol=0)
+        W = Wn
+
+
+def test_adamw_special_cases():
+    rng = np.random.default_rng(24)
+    W = rng.standard_normal(50); G = rng.standard_normal(50); M = rng.standard_normal(50)
+    V = rng.random(50)
+    wo, _, _ = oracle.adamw(W, G, M, V, 0.0, 0.9, 0.999, 1e-8, 0.1, 3)
+    assert np.array_equal(wo, W)
+    Z = np.zeros_like(W)
+    wo, mo, vo = oracle.adamw(W, Z, Z, Z, 1e-3, 0.9, 0.999, 1e-8, 0.1, 1)
+    assert np.array_equal(wo, W * (1 - 1e-4)) and not mo.any() and not vo.any()
