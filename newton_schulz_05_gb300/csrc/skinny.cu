@@ -230,17 +230,19 @@ struct SkinnySmem {
   static constexpr int MP = 8 * MB;
   static constexpr int NP = (MB + 1) / 2;
   static constexpr int MPX = 16 * NP;
-  static constexpr size_t MAT = sizeof(float) * MP * MP;
+  static constexpr size_t MAT = sizeof(float) * MP * MP;             // Gram partials
+  static constexpr int LDM = MP + 1;                                   // padded row of the
+  static constexpr size_t MATP = sizeof(float) * MP * LDM;             // m x m matrices
   // for m > 32 the five m x m matrices reuse the warp-partial region, dead
   // once the CTA partial is formed (NW = 8 >= 5); no ring is used there
   static constexpr bool ALIAS = MB > 4;
   static constexpr size_t gram_w = 0;                       // NW warp partials
   static constexpr size_t mat_a = ALIAS ? 0 : gram_w + NW * MAT;   // A_t
-  static constexpr size_t mat_p = mat_a + MAT;              // P_t
-  static constexpr size_t mat_q = mat_p + MAT;              // Q_t = P_{t-1} ... P_0
-  static constexpr size_t mat_t1 = mat_q + MAT;             // scratch products
-  static constexpr size_t mat_t2 = mat_t1 + MAT;
-  static constexpr size_t gram_c = ALIAS ? gram_w + NW * MAT : mat_t2 + MAT;  // CTA partial
+  static constexpr size_t mat_p = mat_a + MATP;              // P_t
+  static constexpr size_t mat_q = mat_p + MATP;              // Q_t = P_{t-1} ... P_0
+  static constexpr size_t mat_t1 = mat_q + MATP;             // scratch products
+  static constexpr size_t mat_t2 = mat_t1 + MATP;
+  static constexpr size_t gram_c = ALIAS ? gram_w + NW * MAT : mat_t2 + MATP;  // CTA partial
   static constexpr size_t qh = gram_c + MAT;                // fp16 Q, the MMA A operand
   static constexpr size_t bars = (qh + sizeof(__half) * MPX * MPX + 15) & ~size_t(15);
   static constexpr size_t misc = bars + 12 * 8 + 12 * 4;    // 12 mbarriers, 12 counters
@@ -310,10 +312,12 @@ struct MatTile {
 };
 
 // D[i][j] = sum_k A[i][k] B[k][j]  (+ fused P epilogue when MODE == 1:
-// D = c*(A A) + b*A + a*I, with B == A), MP x MP fp32 in shared memory.
+// D = c*(A A) + b*A + a*I, with B == A), MP x MP fp32 in shared memory with
+// rows MP + 1 floats apart.
 template <int MP, int NT, int MODE>
 __device__ __forceinline__ void mat_mul(float* D, const float* A, const float* B, int tid,
                                         float a = 0.f, float b = 0.f, float c = 0.f) {
+  constexpr int LDM = MP + 1;   // padded rows: the A-operand reads of a warp hit distinct banks
   using T = MatTile<MP, NT>;
   constexpr int TB = T::TB, NB = T::NB;
   if (tid >= NB * NB) return;
@@ -329,9 +333,9 @@ __device__ __forceinline__ void mat_mul(float* D, const float* A, const float* B
   for (int k = 0; k < MP; ++k) {
     float av[TB], bv[TB];
     #pragma unroll
-    for (int x = 0; x < TB; ++x) av[x] = (i0 + x < MP) ? A[(i0 + x) * MP + k] : 0.f;
+    for (int x = 0; x < TB; ++x) av[x] = (i0 + x < MP) ? A[(i0 + x) * LDM + k] : 0.f;
     #pragma unroll
-    for (int y = 0; y < TB; ++y) bv[y] = (j0 + y < MP) ? B[k * MP + j0 + y] : 0.f;
+    for (int y = 0; y < TB; ++y) bv[y] = (j0 + y < MP) ? B[k * LDM + j0 + y] : 0.f;
     #pragma unroll
     for (int x = 0; x < TB; ++x)
       #pragma unroll
@@ -344,8 +348,8 @@ __device__ __forceinline__ void mat_mul(float* D, const float* A, const float* B
       const int i = i0 + x, j = j0 + y;
       if (i < MP && j < MP) {
         float v = acc[x][y];
-        if (MODE == 1) v = fmaf(c, v, fmaf(b, A[i * MP + j], i == j ? a : 0.f));
-        D[i * MP + j] = v;
+        if (MODE == 1) v = fmaf(c, v, fmaf(b, A[i * LDM + j], i == j ? a : 0.f));
+        D[i * LDM + j] = v;
       }
     }
 }
@@ -358,7 +362,10 @@ __device__ __forceinline__ void mat_mul(float* D, const float* A, const float* B
 // X_T = (P_{T-1} ... P_0) X_0 = Q X_0.  The iteration is thus carried out
 // exactly on m x m matrices: one pass over the slice forms A_0, the m x m
 // recursion gives Q, one more pass applies O = Q X_0.
-template <int MB, int NW, typename PT>
+// STG: compile the row-streaming (ring) path; the direct path is the general
+// fallback (transposed slices, unaligned rows, m > 32).  Separate
+// instantiations keep the register budget of each path to itself.
+template <int MB, int NW, typename PT, bool STG>
 __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constant__ SkinnyParams p) {
   using S = SkinnySmem<MB, NW, (int)sizeof(PT)>;
   constexpr int MP = S::MP, NP = S::NP, MPX = S::MPX;
@@ -399,7 +406,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   if (st.skip && *st.skip) return;
 
   for (int e = tid; e < MPX * MPX; e += NT) qh[e] = __float2half_rn(0.f);
-  const bool staged = S::STAGED && p.staged;
+  constexpr bool staged = S::STAGED && STG;
   if (tid == 0) {
     for (int b = 0; b < 12; ++b) { mbar_init(&full[b], 1); done_cnt[b] = 0; }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -648,42 +655,36 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     const int src = gram_covered(i, j) ? e : j * MP + i;
     float s = 0.f;
     for (int r = 0; r < p.cluster; ++r) s += cluster.map_shared_rank(gram_c, r)[src];
-    mA[e] = s * inv * inv;                        // A_0 = X_0 X_0^T
-    mQ[e] = i == j ? 1.f : 0.f;
+    mA[i * (MP + 1) + j] = s * inv * inv;         // A_0 = X_0 X_0^T
+    mQ[i * (MP + 1) + j] = i == j ? 1.f : 0.f;
   }
   __syncthreads();
 
   // ---- m x m recursion: P_t = aI + bA_t + cA_t^2;  Q <- P_t Q;  A <- P_t A_t P_t ----
-  // Only the warps that hold product tiles take part; they meet at a named
-  // barrier, the other warps wait at the block barrier below.
   constexpr int NB2 = MatTile<MP, NT>::NB * MatTile<MP, NT>::NB;
-  constexpr bool PAIR = 2 * NB2 <= NT;                 // P Q and P A side by side
-  constexpr int RW = ((PAIR ? 2 * NB2 : NB2) + 31) / 32;
-  auto rsync = [&]() { asm volatile("bar.sync 1, %0;\n" ::"n"(RW * 32) : "memory"); };
-  if (warp < RW) {
-    for (int t = 0; t < st.T; ++t) {
-      mat_mul<MP, NT, 1>(mP, mA, mA, tid, st.a, st.b, st.c);   // P = aI + bA + cA^2
-      rsync();
-      if (PAIR) {
-        if (tid < NB2) mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
-        else if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid - NB2);
-      } else {
-        mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
-        if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid);
-      }
-      rsync();
-      { float* x = mQ; mQ = mT1; mT1 = x; }
-      if (t + 1 < st.T) {
-        mat_mul<MP, NT, 0>(mA, mT2, mP, tid);                  // A <- (P A) P
-        rsync();
-      }
+  for (int t = 0; t < st.T; ++t) {
+    mat_mul<MP, NT, 1>(mP, mA, mA, tid, st.a, st.b, st.c);   // P = aI + bA + cA^2
+    __syncthreads();
+    // Q <- P Q and P A on disjoint thread sets when both fit
+    if (2 * NB2 <= NT) {
+      if (tid < NB2) mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
+      else if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid - NB2);
+    } else {
+      mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
+      if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid);
     }
-    // O = Q X_0 = (Q * inv / sp) (V * sp); the fp16 operand is the scaled Q
-    const float qscale = tot > 0.f ? inv / sp : 0.f;
-    for (int e = tid; e < MP * MP; e += RW * 32) {
-      const int i = e / MP, j = e % MP;
-      qh[i * MPX + j] = __float2half_rn(mQ[e] * qscale);
+    __syncthreads();
+    { float* x = mQ; mQ = mT1; mT1 = x; }
+    if (t + 1 < st.T) {
+      mat_mul<MP, NT, 0>(mA, mT2, mP, tid);                    // A <- (P A) P
+      __syncthreads();
     }
+  }
+  // O = Q X_0 = (Q * inv / sp) (V * sp); the fp16 operand is the scaled Q
+  const float qscale = tot > 0.f ? inv / sp : 0.f;
+  for (int e = tid; e < MP * MP; e += NT) {
+    const int i = e / MP, j = e % MP;
+    qh[i * MPX + j] = __float2half_rn(mQ[i * (MP + 1) + j] * qscale);
   }
   __syncthreads();
   uint32_t afr[NP][NP][4];
@@ -840,7 +841,10 @@ template <int MB, typename PT>
 cudaError_t launch_mb(const Group& g, const SkinnyParams& prm, int nslices, cudaStream_t s) {
   constexpr int NW = MB <= 4 ? 16 : 8;
   using S = SkinnySmem<MB, NW, (int)sizeof(PT)>;
-  auto kern = skinny_kernel<MB, NW, PT>;
+  auto kern = skinny_kernel<MB, NW, PT, false>;
+  if constexpr (S::STAGED) {
+    if (prm.staged) kern = skinny_kernel<MB, NW, PT, true>;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::launch);
   if (e != cudaSuccess) return e;

@@ -2,7 +2,8 @@
 (1-D biases and norm scales, and any other tensor kept off the Muon path),
 one launch for many tensors, against the fp64 oracle element by element.
 
-Tolerances: moments within 1e-6 relative (fp32 storage of fp64 math);
+Tolerances: moments within 1e-6 of the magnitudes of their two terms (fp32
+storage of fp64 math; the terms of m' can cancel);
 parameters within one ulp of the oracle's W' (bf16 round-to-nearest-even)
 plus 4 * 2^-24 of |W (1 - lr wd)| + lr |update| (fp32 intermediates, which
 matter where the two terms cancel), for fp32 parameters the same bound in
@@ -19,6 +20,9 @@ from helpers import bf16_ulp, muon
 pytestmark = pytest.mark.gpu
 
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.1)
+# the hyper-parameters as the library receives them (fp32 through the C ABI):
+# 1 - beta2 of the float 0.999 is 1.3e-5 away from 1e-3
+HP32 = {k: float(np.float32(v)) for k, v in HP.items()}
 SIZES = [1, 3, 24, 1000, 4096, 4097, 10240, 70001, 2 * 4096 * 3 + 5]
 
 
@@ -40,10 +44,13 @@ def _run(dtype, steps=3, sizes=SIZES):
         torch.cuda.synchronize()
         for i in range(len(sizes)):
             # teacher-forced: the oracle starts from the GPU's state of step t-1
-            wo, mo, vo = oracle.adamw(W0[i], G[i], Mr[i], Vr[i], HP["lr"], HP["beta1"],
-                                      HP["beta2"], HP["eps"], HP["wd"], t)
+            wo, mo, vo = oracle.adamw(W0[i], G[i], Mr[i], Vr[i], HP32["lr"], HP32["beta1"],
+                                      HP32["beta2"], HP32["eps"], HP32["wd"], t)
             mg = Md[i].double().cpu().numpy(); vg = Vd[i].double().cpu().numpy()
-            assert np.all(np.abs(mg - mo) <= 1e-6 * np.abs(mo) + 1e-30), (t, i)
+            # the two terms of m' can cancel: bound by their magnitudes
+            gd = G[i].double().numpy()
+            mbound = 1e-6 * (HP32["beta1"] * np.abs(Mr[i]) + (1 - HP32["beta1"]) * np.abs(gd)) + 1e-30
+            assert np.all(np.abs(mg - mo) <= mbound), (t, i)
             assert np.all(np.abs(vg - vo) <= 1e-6 * np.abs(vo) + 1e-38), (t, i)
             wg = Wd[i].double().cpu().numpy()
             w0 = W0[i].double().numpy()
