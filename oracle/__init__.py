@@ -242,3 +242,51 @@ def param_slices(t) -> List:
     if t.dim() == 2:
         return [t]
     return [t[e] for e in range(t.shape[0])]
+
+
+# --------------------------------------------------------------------------
+# assignment of slices to replicas (several GPUs)
+#
+# HyperParallel FSDP Muon RFC, section 4 (HSDP grouped computation): every
+# replica group holds all parameters, each orthogonalises only the ones a
+# greedy algorithm assigns to it for an even compute load, and the updated
+# parameters are then broadcast; section 2: the E slices of an [E, M, N]
+# expert tensor are mathematically independent, so a slice is the unit.
+# Readings (the RFC names the algorithm "greedy" and the goal "balanced
+# compute", nothing more):
+#   * the load of a slice is its time on the roofline of one GPU,
+#     max(Newton-Schulz flops / tensor rate, optimizer-state bytes / HBM rate),
+#     flops in the standard count T (4 m^2 n + 2 m^3) (X X^T and B X at
+#     2 m^2 n each, A A at 2 m^3 per step), bytes 3 es + 8 per element
+#     (G read, W read and written in the parameter dtype; fp32 momentum read
+#     and written);
+#   * greedy = longest first: slices in decreasing load (equal loads: lower
+#     global slice id first), each to the replica with the least load so far
+#     (equal: the lower rank).
+def slice_costs(shapes: Sequence[Tuple[int, ...]], dtypes: Sequence[str], ns_steps: int,
+                flops_per_s: float, bytes_per_s: float) -> List[float]:
+    """Load (seconds) of every slice, in global slice order."""
+    costs = []
+    for shape, dt in zip(shapes, dtypes):
+        E, M, N = (1, shape[0], shape[1]) if len(shape) == 2 else tuple(shape)
+        m, n = min(M, N), max(M, N)
+        es = 2 if dt == "bf16" else 4
+        flops = ns_steps * (4 * m * m * n + 2 * m * m * m)     # exact Python integers
+        nbytes = m * n * (3 * es + 8)
+        cost = max(flops / flops_per_s, nbytes / bytes_per_s)
+        costs.extend([cost] * E)
+    return costs
+
+
+def partition(costs: Sequence[float], world: int) -> Tuple[List[int], List[float]]:
+    """Greedy longest-first assignment of slices to `world` replicas.
+
+    Returns (owner of each slice, summed load of each replica)."""
+    order = sorted(range(len(costs)), key=lambda s: (-costs[s], s))
+    load = [0.0] * world
+    owner = [0] * len(costs)
+    for s in order:
+        r = min(range(world), key=lambda k: (load[k], k))
+        owner[s] = r
+        load[r] += costs[s]
+    return owner, load
