@@ -389,14 +389,23 @@ def run_ours(args, w):
                 "note": "standard NS flops over the whole step; peak bf16 burst %s" % (
                     "of measured" if pk["src"] == "measured" else "of fallback")}
 
+    # operand types of the tensor-core products: the fused skinny kernel takes
+    # bf16 V and bf16 Q (fp32 m x m recursion), the dense path fp16 iterates
+    if kinds == {mu.KERNEL_SKINNY}:
+        arith, mode = "bf16", "bf16 tensor-core operands, fp32 accumulate, fp32 m x m recursion"
+    elif mu.KERNEL_SKINNY in kinds:
+        arith, mode = "f16", ("fp16 tensor-core operands (dense groups), bf16 (skinny groups), "
+                              "fp32 accumulate")
+    else:
+        arith, mode = "f16", "fp16 tensor-core operands, fp32 accumulate"
     out = {"metric": METRIC, "value": weak_scaling_value(n_slices, ws_n, ms), "unit": UNIT,
            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": "f16", "data": "synthetic",
+           "dtype": arith, "data": "synthetic",
            "config": {"workload": w.name, "slices": n_slices, "param_dtype": str(w.dtype),
                       "ns_steps": w.ns_steps, "l2": "flushed (512 MB write) before each timed step",
                       "parallelism": "replica per GPU" if ws_n > 1 else "single GPU",
-                      "mode": "fp16 tensor-core operands, fp32 accumulate"},
+                      "mode": mode},
            "roofline": roof,
            "e2e": {"value": weak_scaling_value(n_slices, ws_n, ms_e2e), "unit": UNIT,
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -23,10 +23,11 @@
 //     of a warp-MMA fragment, so the slice never returns to HBM: traffic is
 //     G + M read, M' written, W read and W' written, 14 B per element for
 //     bf16 parameters;
-//   * V V^T (bf16 operands) and Q X_0 (fp16 operands: X_0 is V times a power
-//     of two, exact) run on the tensor cores as m16n8k16 / m16n8k8 warp MMAs
-//     with fp32 accumulation; Q X_0 takes X_0 as its B operand through
-//     movmatrix transposes of the 8x8 register blocks;
+//   * V V^T and Q X_0 = (Q / (||V|| + eps)) V run on the tensor cores as
+//     bf16 m16n8k16 / m16n8k8 warp MMAs with fp32 accumulation: the bf16 V
+//     held in TMEM is the B operand of both (through movmatrix transposes of
+//     its 8x8 register blocks for the second), the normalisation is folded
+//     into the fp32 Q before it is rounded to bf16;
 //   * ||V||^2 and V V^T are reduced deterministically: warps -> CTA in shared
 //     memory, CTAs -> cluster through distributed shared memory in rank
 //     order, so every CTA holds the same bits and computes the same Q in fp32;
@@ -67,10 +68,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ uint32_t pack_h(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
   return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
 }
@@ -79,22 +76,6 @@ __device__ __forceinline__ uint32_t movt(uint32_t a) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
   return d;
 }
-__device__ __forceinline__ void mma_k16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_k8(float* d, uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(b0));
-}
-
 // tensor memory: 32 lanes x 4 columns per warp access (lane = thread)
 __device__ __forceinline__ void tm_ld4(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
@@ -243,8 +224,8 @@ struct SkinnySmem {
   static constexpr size_t mat_t1 = mat_q + MATP;             // scratch products
   static constexpr size_t mat_t2 = mat_t1 + MATP;
   static constexpr size_t gram_c = ALIAS ? gram_w + NW * MAT : mat_t2 + MATP;  // CTA partial
-  static constexpr size_t qh = gram_c + MAT;                // fp16 Q, the MMA A operand
-  static constexpr size_t bars = (qh + sizeof(__half) * MPX * MPX + 15) & ~size_t(15);
+  static constexpr size_t qh = gram_c + MAT;                // bf16 Q, the MMA A operand
+  static constexpr size_t bars = (qh + sizeof(__nv_bfloat16) * MPX * MPX + 15) & ~size_t(15);
   static constexpr size_t misc = bars + 12 * 8 + 12 * 4;    // 12 mbarriers, 12 counters
   static constexpr size_t ring = (misc + 64 * sizeof(float) + 16 + 127) & ~size_t(127);
   // ring of row stages (bulk copies), SW columns = one superchunk per warp;
@@ -282,6 +263,14 @@ __device__ __forceinline__ void mma_k16_bf16(float* d, uint32_t a0, uint32_t a1,
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_k8_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
 }
 
 // X X^T partial of one superchunk (bf16 fragments, fp32 accumulation)
@@ -382,7 +371,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   float* mQ = reinterpret_cast<float*>(smem + S::mat_q);
   float* mT1 = reinterpret_cast<float*>(smem + S::mat_t1);
   float* mT2 = reinterpret_cast<float*>(smem + S::mat_t2);
-  __half* qh = reinterpret_cast<__half*>(smem + S::qh);
+  __nv_bfloat16* qh = reinterpret_cast<__nv_bfloat16*>(smem + S::qh);
   float* red = reinterpret_cast<float*>(smem + S::misc);     // NW floats
   float* norm_slot = red + 32;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 48);
@@ -405,7 +394,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   // a loss-scaled step whose gradients hold an inf or NaN changes nothing
   if (st.skip && *st.skip) return;
 
-  for (int e = tid; e < MPX * MPX; e += NT) qh[e] = __float2half_rn(0.f);
+  for (int e = tid; e < MPX * MPX; e += NT) qh[e] = __float2bfloat16_rn(0.f);
   constexpr bool staged = S::STAGED && STG;
   if (tid == 0) {
     for (int b = 0; b < 12; ++b) { mbar_init(&full[b], 1); done_cnt[b] = 0; }
@@ -646,10 +635,6 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   float tot = 0.f;
   for (int r = 0; r < p.cluster; ++r) tot += *cluster.map_shared_rank(norm_slot, r);
   const float inv = 1.f / (sqrtf(tot) + st.eps);
-  // X0 = V * 2^-e exactly (power of two near 1/||V||): bf16 -> fp16 loses nothing
-  int ex = 0;
-  frexpf(sqrtf(tot), &ex);
-  const float sp = ldexpf(1.f, -ex);
   for (int e = tid; e < MP * MP; e += NT) {
     const int i = e / MP, j = e % MP;
     const int src = gram_covered(i, j) ? e : j * MP + i;
@@ -680,11 +665,11 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
       __syncthreads();
     }
   }
-  // O = Q X_0 = (Q * inv / sp) (V * sp); the fp16 operand is the scaled Q
-  const float qscale = tot > 0.f ? inv / sp : 0.f;
+  // O = Q X_0 = (Q * inv) V; the bf16 A operand is the scaled Q
+  const float qscale = tot > 0.f ? inv : 0.f;
   for (int e = tid; e < MP * MP; e += NT) {
     const int i = e / MP, j = e % MP;
-    qh[i * MPX + j] = __float2half_rn(mQ[i * (MP + 1) + j] * qscale);
+    qh[i * MPX + j] = __float2bfloat16_rn(mQ[i * (MP + 1) + j] * qscale);
   }
   __syncthreads();
   uint32_t afr[NP][NP][4];
@@ -692,8 +677,8 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   for (int P = 0; P < NP; ++P)
     #pragma unroll
     for (int kk = 0; kk < NP; ++kk) {
-      const __half* r0 = qh + (16 * P + g) * MPX + 16 * kk + 2 * t4;
-      const __half* r1 = r0 + 8 * MPX;
+      const __nv_bfloat16* r0 = qh + (16 * P + g) * MPX + 16 * kk + 2 * t4;
+      const __nv_bfloat16* r1 = r0 + 8 * MPX;
       afr[P][kk][0] = *reinterpret_cast<const uint32_t*>(r0);
       afr[P][kk][1] = *reinterpret_cast<const uint32_t*>(r1);
       afr[P][kk][2] = *reinterpret_cast<const uint32_t*>(r0 + 8);
@@ -766,13 +751,6 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
       #pragma unroll
       for (int rb = 0; rb < MB; ++rb) tm_ld4(taddr_w + (q + 1) * 4 * MB + 4 * rb, xn[rb]);
     }
-    #pragma unroll
-    for (int rb = 0; rb < MB; ++rb)
-      #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float2 f = unpack_bf16(xr[rb][r]);
-        xr[rb][r] = pack_h(f.x * sp, f.y * sp);
-      }
     float o[MB][4][2];
     #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -785,10 +763,10 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
         #pragma unroll
         for (int kk = 0; kk < NP; ++kk) {
           if (2 * kk + 1 < MB)
-            mma_k16(y, afr[P][kk][0], afr[P][kk][1], afr[P][kk][2], afr[P][kk][3], xt[2 * kk],
+            mma_k16_bf16(y, afr[P][kk][0], afr[P][kk][1], afr[P][kk][2], afr[P][kk][3], xt[2 * kk],
                     xt[(2 * kk + 1) % MB]);
           else
-            mma_k8(y, afr[P][kk][0], afr[P][kk][1], xt[2 * kk]);
+            mma_k8_bf16(y, afr[P][kk][0], afr[P][kk][1], xt[2 * kk]);
         }
         o[2 * P][r][0] = y[0];
         o[2 * P][r][1] = y[1];
