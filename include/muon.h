@@ -231,6 +231,36 @@ MUON_API muon_status muon_step_static(const muon_plan_t* plan, void* const* para
  * accounting; no device call). */
 MUON_API muon_status muon_plan_launches(const muon_plan_t* plan, int ns_steps, int* out);
 
+/*
+ * Assignment of the plan's slices to `world` replicas that all hold every
+ * parameter (HyperParallel FSDP Muon RFC, section 4, HSDP grouped
+ * computation: each replica group orthogonalises only the parameters that a
+ * greedy algorithm assigns to it for an even compute load, then the updated
+ * parameters are broadcast; section 2: the E slices of an [E, M, N] tensor
+ * are independent, so the unit of assignment is a slice).  Host only, no
+ * device call; the result depends only on the plan's shapes and the
+ * arguments, so every replica computes the same assignment without
+ * communicating.
+ *
+ * Load of a slice (seconds on the roofline of one GPU):
+ *   max(T (4 m^2 n + 2 m^3) / flops_per_s,  m n (3 es + 8) / bytes_per_s)
+ * with m = min(M, N), n = max(M, N), T = ns_steps, es = 2 (bf16) or 4 (fp32):
+ * standard Newton-Schulz flop count, and the optimizer state touched once
+ * (gradient read, parameter read and written, fp32 momentum read and
+ * written).  Greedy longest first: slices in decreasing load (equal loads:
+ * lower global slice id first), each to the replica with the least summed
+ * load so far (equal sums: lower rank).
+ *   owner      host, muon_plan_num_slices ints, written: owner[s] is the rank
+ *              of global slice s (parameters in plan order, slices e = 0..E-1
+ *              of each)
+ *   rank_load  host, `world` doubles, written, or null: summed load per rank
+ * Errors: MUON_ERR_INVALID_ARG for a null plan or owner, world < 1,
+ * ns_steps < 0, or a rate that is not finite and positive.
+ */
+MUON_API muon_status muon_plan_partition(const muon_plan_t* plan, int world, int ns_steps,
+                                         double flops_per_s, double bytes_per_s, int* owner,
+                                         double* rank_load);
+
 MUON_API void muon_plan_destroy(muon_plan_t* plan);
 MUON_API const char* muon_status_string(muon_status s);
 

@@ -58,9 +58,15 @@ EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
            "muon_plan_num_groups", "muon_plan_num_slices", "muon_plan_group",
            "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
            "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static",
-           "muon_step_amp", "muon_adamw_step"]
+           "muon_step_amp", "muon_adamw_step", "muon_plan_partition"]
 
 STATIC_WORKSPACE_BYTES = 32 << 20   # MUON_STATIC_WORKSPACE_BYTES in include/muon.h
+
+# default rates of the slice loads of Plan.partition: dense fp16/bf16 tensor
+# throughput and STREAM-copy HBM bandwidth of one GB300, as measured (only
+# their ratio matters to the assignment)
+GB300_FLOPS = 1.88e15
+GB300_HBM_BYTES = 6.78e12
 
 _lib = None
 
@@ -96,6 +102,9 @@ def load(path: str = LIB_PATH):
                                   ctypes.c_float, ctypes.c_float, ctypes.c_int, vp]
     L.muon_workspace_error.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.muon_plan_launches.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    L.muon_plan_partition.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                      ctypes.c_double, ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(ctypes.c_double)]
     L.muon_plan_destroy.argtypes = [vp]
     L.muon_plan_destroy.restype = None
     L.muon_status_string.argtypes = [ctypes.c_int]
@@ -103,7 +112,7 @@ def load(path: str = LIB_PATH):
     for fn in ("muon_plan", "muon_plan_workspace_bytes", "muon_plan_num_groups",
                "muon_plan_num_slices", "muon_plan_group", "muon_plan_slice", "muon_step",
                "muon_step_ortho", "muon_workspace_error", "muon_plan_launches",
-               "muon_step_static", "muon_step_amp", "muon_adamw_step"):
+               "muon_step_static", "muon_step_amp", "muon_adamw_step", "muon_plan_partition"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -197,6 +206,17 @@ class Plan:
         v = ctypes.c_int()
         _check(load().muon_plan_launches(self._h, ns_steps, ctypes.byref(v)), "plan_launches")
         return v.value
+
+    def partition(self, world: int, ns_steps: int = 5, flops_per_s: float = GB300_FLOPS,
+                  bytes_per_s: float = GB300_HBM_BYTES) -> Tuple[List[int], List[float]]:
+        """muon_plan_partition: owner rank of every global slice and the summed
+        load (seconds) of every rank."""
+        ns = self.num_slices
+        owner = (ctypes.c_int * max(ns, 1))()
+        loads = (ctypes.c_double * max(world, 1))()
+        _check(load().muon_plan_partition(self._h, world, ns_steps, flops_per_s, bytes_per_s,
+                                          owner, loads), "plan_partition")
+        return list(owner[:ns]), list(loads[:world])
 
 
 def _ptrs(ts) -> ctypes.Array:
@@ -375,3 +395,106 @@ class PreparedStep:
 
     def __call__(self) -> None:
         _check(self._fn(*self._args), "muon_step")
+
+
+class Partition:
+    """Slices of a set of parameters dealt to `world` replicas that all hold
+    every parameter (HyperParallel FSDP Muon RFC, section 4: each replica
+    orthogonalises the parameters a greedy algorithm assigns to it, then the
+    updated parameters are broadcast; section 2: a slice of an [E, M, N]
+    tensor is the unit).  Owners come from muon_plan_partition, so every
+    replica computes the same assignment without communicating.
+
+    ``broadcast`` sends each rank's updated slices to the others through
+    torch.distributed (one broadcast per owner and dtype of a packed buffer);
+    it moves bytes only."""
+
+    def __init__(self, plan: Plan, world: int, ns_steps: int = 5,
+                 flops_per_s: float = GB300_FLOPS, bytes_per_s: float = GB300_HBM_BYTES):
+        self.world = world
+        self.owner, self.rank_load = plan.partition(world, ns_steps, flops_per_s, bytes_per_s)
+        # global slice id -> (param, e)
+        self.slice_keys = []
+        for p, shape in enumerate(plan.shapes):
+            for e in range(shape[0] if len(shape) == 3 else 1):
+                self.slice_keys.append((p, e))
+        self._bufs = {}
+
+    def owned(self, rank: int) -> List[Tuple[int, int]]:
+        """(param, slice) pairs of `rank`, in global slice order."""
+        return [k for k, o in zip(self.slice_keys, self.owner) if o == rank]
+
+    @staticmethod
+    def view(t: torch.Tensor, key: Tuple[int, int]) -> torch.Tensor:
+        """The 2-D [M, N] slice `key` = (param, e) of the list's tensor."""
+        return t if t.dim() == 2 else t[key[1]]
+
+    def views(self, tensors: Sequence[torch.Tensor], rank: int) -> List[torch.Tensor]:
+        return [self.view(tensors[p], (p, e)) for p, e in self.owned(rank)]
+
+    def broadcast(self, params: Sequence[torch.Tensor], group=None) -> None:
+        """Every rank's slices of `params` sent from that rank to all others."""
+        import torch.distributed as dist
+        if self.world == 1:
+            return
+        me = dist.get_rank(group) if group is not None else dist.get_rank()
+        for r in range(self.world):
+            vs = self.views(params, r)
+            by_dtype = {}
+            for v in vs:
+                by_dtype.setdefault(v.dtype, []).append(v)
+            for dt, lst in by_dtype.items():
+                total = sum(v.numel() for v in lst)
+                key = (r, dt, lst[0].device)
+                buf = self._bufs.get(key)
+                if buf is None or buf.numel() != total:
+                    buf = torch.empty(total, dtype=dt, device=lst[0].device)
+                    self._bufs[key] = buf
+                if me == r:
+                    torch.cat([v.reshape(-1) for v in lst], out=buf)
+                src = dist.get_global_rank(group, r) if group is not None else r
+                dist.broadcast(buf, src=src, group=group)
+                if me != r:
+                    off = 0
+                    for v in lst:
+                        v.copy_(buf[off:off + v.numel()].view_as(v))
+                        off += v.numel()
+
+
+class ShardedMuon:
+    """Muon over the replicas of a process group: every rank holds all
+    parameters and the full (already reduced) gradients, orthogonalises and
+    updates only the slices the Partition gives it, keeps fp32 momentum for
+    those slices only, then the updated slices are broadcast from their
+    owners.  The update on each rank runs in libmuon's kernels over a plan of
+    the rank's own 2-D slice views; the result equals the single-replica step
+    slice for slice (every slice is computed independently of the others)."""
+
+    def __init__(self, params: Sequence[torch.Tensor], rank: int, world: int, group=None,
+                 lr: float = 0.02, beta: float = 0.95, wd: float = 0.1, nesterov: bool = True,
+                 ns_steps: int = 5, coeffs=DEFAULT_COEFFS, mode: str = "tc16", eps: float = 1e-7,
+                 flops_per_s: float = GB300_FLOPS, bytes_per_s: float = GB300_HBM_BYTES):
+        self.params = list(params)
+        self.rank, self.world, self.group = rank, world, group
+        self.partition = Partition(Plan(self.params, mode=mode, eps=eps), world, ns_steps,
+                                   flops_per_s, bytes_per_s)
+        self.owned = self.partition.owned(rank)
+        self.param_views = self.partition.views(self.params, rank)
+        self.plan = Plan(self.param_views, mode=mode, eps=eps)
+        self.momentum = [torch.zeros(v.shape, dtype=torch.float32, device=v.device)
+                         for v in self.param_views]
+        dev = self.params[0].device if self.params else None
+        self.workspace = alloc_workspace(self.plan, dev)
+        self.hp = dict(lr=lr, beta=beta, wd=wd, nesterov=nesterov, ns_steps=ns_steps,
+                       coeffs=coeffs)
+
+    def update_owned(self, grads: Sequence[torch.Tensor], stream=None) -> None:
+        """The step on this rank's slices only (no communication)."""
+        if self.param_views:
+            step(self.plan, self.param_views, self.partition.views(grads, self.rank),
+                 self.momentum, workspace=self.workspace, stream=stream, **self.hp)
+
+    def step(self, grads: Sequence[torch.Tensor], stream=None) -> None:
+        self.update_owned(grads, stream)
+        if self.world > 1:
+            self.partition.broadcast(self.params, self.group)

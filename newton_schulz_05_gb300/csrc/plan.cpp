@@ -6,9 +6,12 @@
 // device sees one batched launch sequence per shape instead of one per
 // matrix; section 2: an [E, M, N] tensor contributes E independent slices.
 // The plan is built once, on the host, with no device call.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <new>
+#include <queue>
+#include <utility>
 
 #include "internal.h"
 
@@ -201,6 +204,50 @@ muon_status muon_plan_launches(const muon_plan_t* P, int ns_steps, int* out) {
     }
   }
   *out = n;
+  return MUON_OK;
+}
+
+muon_status muon_plan_partition(const muon_plan_t* P, int world, int ns_steps,
+                                double flops_per_s, double bytes_per_s, int* owner,
+                                double* rank_load) {
+  if (!P || !owner || world < 1 || ns_steps < 0) return MUON_ERR_INVALID_ARG;
+  if (!std::isfinite(flops_per_s) || !(flops_per_s > 0.0) || !std::isfinite(bytes_per_s) ||
+      !(bytes_per_s > 0.0))
+    return MUON_ERR_INVALID_ARG;
+  // per-group load: counts in 128-bit integers, one rounding to double each
+  std::vector<double> group_load(P->groups.size());
+  for (size_t k = 0; k < P->groups.size(); ++k) {
+    const Group& G = P->groups[k];
+    const unsigned __int128 m = (unsigned __int128)G.m, n = (unsigned __int128)G.n;
+    const unsigned __int128 flops = (unsigned __int128)ns_steps * (4 * m * m * n + 2 * m * m * m);
+    const unsigned __int128 bytes = m * n * (unsigned __int128)(G.dtype == MUON_BF16 ? 14 : 20);
+    const double tf = (double)flops / flops_per_s;
+    const double tb = (double)bytes / bytes_per_s;
+    group_load[k] = tf > tb ? tf : tb;
+  }
+  const int ns = (int)P->slice_group.size();
+  std::vector<int> order(ns);
+  for (int s = 0; s < ns; ++s) order[s] = s;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    return group_load[P->slice_group[a]] > group_load[P->slice_group[b]];
+  });
+  // least loaded rank first, the lower rank among equals
+  using Entry = std::pair<double, int>;
+  std::priority_queue<Entry, std::vector<Entry>, std::greater<Entry>> heap;
+  for (int r = 0; r < world; ++r) heap.push({0.0, r});
+  for (int s : order) {
+    Entry e = heap.top();
+    heap.pop();
+    owner[s] = e.second;
+    e.first += group_load[P->slice_group[s]];
+    heap.push(e);
+  }
+  if (rank_load) {
+    while (!heap.empty()) {
+      rank_load[heap.top().second] = heap.top().first;
+      heap.pop();
+    }
+  }
   return MUON_OK;
 }
 

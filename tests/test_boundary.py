@@ -188,3 +188,58 @@ def test_adamw_rejects_bad_arguments(muon):
     assert L.muon_adamw_step(*args(dt=5)) == -3
     assert L.muon_adamw_step(*args(n=-1)) == -1
     assert L.muon_adamw_step(0, None, None, None, None, None, 0, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, None) == 0
+
+
+def _oracle_partition(plan, world, T, fr, br):
+    dts = ["bf16" if d == 0 else "f32" for d in plan.dtypes]
+    return oracle.partition(oracle.slice_costs(plan.shapes, dts, T, fr, br), world)
+
+
+def test_partition_matches_oracle_random(muon):
+    import torch
+    rng = np.random.default_rng(5)
+    dims = [1, 7, 24, 64, 65, 130, 1408, 4096]
+    for _ in range(40):
+        shapes = []
+        for _ in range(rng.integers(1, 12)):
+            if rng.random() < 0.4:
+                shapes.append(((int(rng.integers(1, 6)), int(rng.choice(dims)), int(rng.choice(dims))),
+                               torch.bfloat16 if rng.random() < 0.7 else torch.float32))
+            else:
+                shapes.append(((int(rng.choice(dims)), int(rng.choice(dims))),
+                               torch.bfloat16 if rng.random() < 0.7 else torch.float32))
+        plan = muon.Plan(shapes)
+        world = int(rng.integers(1, 9))
+        T = int(rng.integers(0, 8))
+        fr, br = float(rng.choice([1.88e15, 1e9, 1.0])), float(rng.choice([6.78e12, 1e9, 14.0]))
+        owner, load = plan.partition(world, T, fr, br)
+        o_owner, o_load = _oracle_partition(plan, world, T, fr, br)
+        assert owner == o_owner
+        assert [struct.pack("<d", x) for x in load] == [struct.pack("<d", x) for x in o_load]
+
+
+@pytest.mark.parametrize("name", ["skinny_74x24x10240", "stacks_experts", "dense_24L", "moe_24L"])
+@pytest.mark.parametrize("world", [2, 8])
+def test_partition_matches_oracle_on_workloads(muon, name, world):
+    import synth
+    w = synth.workload(name)
+    plan = muon.Plan([(s, w.dtype) for s in w.shapes])
+    owner, load = plan.partition(world, w.ns_steps)
+    o_owner, o_load = _oracle_partition(plan, world, w.ns_steps, muon.GB300_FLOPS,
+                                        muon.GB300_HBM_BYTES)
+    assert owner == o_owner and load == o_load
+    assert sorted(set(owner)) == list(range(world))
+
+
+def test_partition_rejects_bad_arguments(muon):
+    import torch
+    plan = muon.Plan([((24, 64), torch.bfloat16)])
+    L = muon.load()
+    own = (ctypes.c_int * 1)()
+    assert L.muon_plan_partition(plan.handle, 0, 5, 1e15, 1e12, own, None) == -1
+    assert L.muon_plan_partition(plan.handle, 2, -1, 1e15, 1e12, own, None) == -1
+    assert L.muon_plan_partition(plan.handle, 2, 5, 0.0, 1e12, own, None) == -1
+    assert L.muon_plan_partition(plan.handle, 2, 5, 1e15, float("inf"), own, None) == -1
+    assert L.muon_plan_partition(plan.handle, 2, 5, 1e15, 1e12, None, None) == -1
+    assert L.muon_plan_partition(None, 2, 5, 1e15, 1e12, own, None) == -1
+    assert L.muon_plan_partition(plan.handle, 3, 5, 1e15, 1e12, own, None) == 0 and own[0] == 0
