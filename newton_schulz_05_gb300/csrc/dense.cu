@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kNT) epilogue_kernel(
 }
 
 struct Offsets {
-  size_t V, X0, X1, A, B, part, inv;
+  size_t V, X0, X1, A, A2, B, part, inv;
 };
 
 Offsets dense_offsets(const Group& g, int mode) {
@@ -254,6 +254,7 @@ Offsets dense_offsets(const Group& g, int mode) {
   o.X0 = p; p += a256(e * mp * np);
   o.X1 = p; p += a256(e * mp * np);
   o.A = p;  p += a256(e * mp * mp);
+  o.A2 = p; p += mode == MUON_MODE_FP32 ? 0 : a256(e * mp * mp);   // c A + b I (tensor-core path)
   o.B = p;  p += a256(e * mp * mp);
   o.part = p; p += a256(4 * (mp / kFrontTileR) * (np / kFrontTileC));
   o.inv = p; p += 256;
@@ -292,29 +293,34 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
                                                      st.T == 0 ? 1 : 0);
   size_t xin = off.X0, xout = off.X1;
   if constexpr (sizeof(IT) == 2) {
-    // fp16 operands: the three products on the tcgen05 tensor cores
+    // fp16 operands: the three products on the tcgen05 tensor cores.  The
+    // a and b terms of the step are folded into the operands, so that no
+    // product reads a third matrix:  b A + c A A = A (c A + b I)  and
+    // a X + B X = (B + a I) X.  Padded rows and columns of X are zero, so the
+    // identity entries past m meet only zeros.
     for (int t = 0; t < st.T; ++t) {
       const bool last = t == st.T - 1;
       TcGemm g1;
       g1.batch = ns; g1.stride = sws; g1.err = err_word; g1.skip = st.skip;
-      // A = X X^T (symmetric)
+      // A = X X^T and A2 = c X X^T + b I (symmetric)
       g1.M = mp; g1.N = mp; g1.K = np;
       g1.A = ws + xin; g1.B = ws + xin; g1.D = ws + off.A; g1.sym = 1;
+      g1.D2 = ws + off.A2; g1.alpha2 = st.c; g1.diag2 = st.b;
       cudaError_t e = tc_gemm(g1, s);
       if (e != cudaSuccess) return e;
-      // B = c*A*A + b*A (symmetric; A A = A A^T)
-      TcGemm g2 = g1;
-      g2.K = mp;
-      g2.A = ws + off.A; g2.B = ws + off.A; g2.C = ws + off.A; g2.D = ws + off.B;
-      g2.alpha = st.c; g2.beta = st.b;
+      // B' = A A2 + a I = b A + c A A + a I (symmetric: A and A2 commute)
+      TcGemm g2;
+      g2.batch = ns; g2.stride = sws; g2.err = err_word; g2.skip = st.skip;
+      g2.M = mp; g2.N = mp; g2.K = mp;
+      g2.A = ws + off.A; g2.B = ws + off.A2; g2.D = ws + off.B; g2.sym = 1;
+      g2.diag = st.a;
       e = tc_gemm(g2, s);
       if (e != cudaSuccess) return e;
-      // X' = B X + a*X, X as an N-major B operand; fp32 O on the last step
+      // X' = B' X, X as an N-major B operand; fp32 O on the last step
       TcGemm g3;
       g3.batch = ns; g3.stride = sws; g3.err = err_word; g3.skip = st.skip;
       g3.M = mp; g3.N = np; g3.K = mp;
-      g3.A = ws + off.B; g3.B = ws + xin; g3.C = ws + xin; g3.b_mn = 1;
-      g3.alpha = 1.f; g3.beta = st.a;
+      g3.A = ws + off.B; g3.B = ws + xin; g3.b_mn = 1;
       g3.D = ws + (last ? off.V : xout); g3.d_f32 = last ? 1 : 0;
       e = tc_gemm(g3, s);
       if (e != cudaSuccess) return e;

@@ -27,6 +27,7 @@ size_t dense_slice_ws(const Group& g, int mode) {
   b += align256(4 * mp * np);       // V (front output), then O (last update)
   b += 2 * align256(e * mp * np);   // X ping-pong
   b += 2 * align256(e * mp * mp);   // A and B
+  if (mode != MUON_MODE_FP32) b += align256(e * mp * mp);   // c A + b I
   const size_t nblk = (size_t)(mp / kFrontTileR) * (size_t)(np / kFrontTileC);
   b += align256(4 * nblk);          // front partial sums of squares
   b += 256;                         // per-slice 1/(||V|| + eps)

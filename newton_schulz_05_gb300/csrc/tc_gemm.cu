@@ -1,18 +1,24 @@
 // Batched fp16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA)
-// for the dense Newton-Schulz products:
-//   A = X X^T          (symmetric output: upper tiles only, mirrored)
-//   B = c*A*A + b*A    (symmetric output, C = A)
-//   X' = B*X + a*X     (B operand N-major, C = X; fp32 output on the last step)
-// D[b] = alpha * A[b] op(B[b]) + beta * C[b], fp32 accumulation in TMEM.
+// for the dense Newton-Schulz products of one step, with the a, b terms of
+// the polynomial folded into the operands so no product reads a third matrix:
+//   A = X X^T, A2 = c X X^T + b I   (symmetric: upper tiles only, mirrored;
+//                                    two outputs of one accumulator)
+//   B' = A A2 + a I                 (symmetric; = b A + c A A + a I)
+//   X' = B' X                       (B operand N-major; fp32 on the last step)
+// D[b] = alpha * A[b] op(B[b]) + diag * I (and D2 = alpha2 * A op(B) + diag2 * I),
+// fp32 accumulation in TMEM.
 //
 // One persistent CTA per SM, 6 warps:
 //   warp 0    TMA producer: 128x64 A box and 256x64 B box per stage (or four
 //             64x64 N-major boxes), 4-stage ring, 128-byte swizzle;
 //   warp 1    allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
 //             one thread issues tcgen05.mma (M=128, N=256, K=16);
-//   warps 2-5 epilogue: tcgen05.ld of their 32 TMEM lanes, alpha/beta, store;
-//             the accumulator is double-buffered so the epilogue of tile t
-//             overlaps the MMAs of tile t+1.
+//   warps 2-5 epilogue: tcgen05.ld of their 32 TMEM lanes (rows), scaled rows
+//             written to a shared-memory staging tile and sent to global
+//             memory by TMA tensor stores (32 x 32 boxes; the mirror of a
+//             symmetric tile as a transposed staging tile); the accumulator is
+//             double-buffered so the epilogue of tile t overlaps the MMAs of
+//             tile t+1.
 // Every mbarrier wait is bounded; when a budget runs out the kernel records
 // an error word, drains its own copies in flight and returns.
 #include <cuda.h>
@@ -34,16 +40,16 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int NTHREADS = 192;
+constexpr int EPI_BYTES = 8192;                 // staging bytes per epilogue warp
 constexpr uint32_t kWaitLimit = 1u << 26;       // try_wait polls before giving up
 
 struct TcParams {
   int M, N, K;
   int tiles_m, tiles_n, tiles_per_batch, total_tiles;
-  size_t stride;       // bytes between batch entries (C and D)
-  const __half* C;     // [M, N] of batch 0, or null
-  void* D;             // [M, N] of batch 0
-  int d_f32;
-  float alpha, beta;
+  int d_f32;           // D in fp32 (else fp16)
+  int has_d2;          // second fp16 output D2
+  float alpha, diag;   // D  = alpha  * acc + diag  * I
+  float alpha2, diag2; // D2 = alpha2 * acc + diag2 * I
   int sym;
   int b_mn;
   uint32_t idesc;
@@ -89,6 +95,71 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "%4, %5}], [%2];\n" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// wait until at most n bulk groups of this thread still read shared memory
+__device__ __forceinline__ void bulk_wait_read(int n) {
+  if (n >= 3) asm volatile("cp.async.bulk.wait_group.read 3;\n" ::: "memory");
+  else if (n == 1) asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
+  else asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t a, __half h) {
+  asm volatile("st.shared.b16 [%0], %1;\n" ::"r"(a), "h"(__half_as_ushort(h)) : "memory");
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// Staging tiles of 32 x 32 outputs, laid out as the TMA tensor store reads
+// them with swizzling: fp16 tiles (64-byte rows) with the 64-byte pattern,
+// 16-byte piece j of row r at position j ^ ((r >> 1) & 3); fp32 tiles
+// (128-byte rows) with the 128-byte pattern, piece j at j ^ (r & 7).  The 32
+// lanes of a warp (one row each) then spread over all shared-memory banks.
+// Tiles start on 1024-byte boundaries.
+__device__ __forceinline__ void stage_row_h(uint32_t tile, int r, const float* v) {
+  #pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float* x = v + 8 * j;
+    sts128(tile + r * 64 + ((j ^ ((r >> 1) & 3)) << 4), pack_h2(x[0], x[1]), pack_h2(x[2], x[3]),
+           pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
+  }
+}
+__device__ __forceinline__ void stage_row_f(uint32_t tile, int r, const float* v) {
+  #pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float* x = v + 4 * j;
+    sts128(tile + r * 128 + ((j ^ (r & 7)) << 4), __float_as_uint(x[0]), __float_as_uint(x[1]),
+           __float_as_uint(x[2]), __float_as_uint(x[3]));
+  }
+}
+// column r of a transposed fp16 staging tile (the mirror of row r): element
+// (j, r) of the tile, in piece r / 8 of row j
+__device__ __forceinline__ void stage_col_h(uint32_t tile, int r, const float* v) {
+  const uint32_t within = (uint32_t)(r & 7) * 2;
+  #pragma unroll
+  for (int j = 0; j < 32; ++j)
+    sts16(tile + j * 64 + ((((r >> 3) ^ ((j >> 1) & 3))) << 4) + within, __float2half_rn(v[j]));
 }
 
 // shared-memory matrix descriptor, 128-byte swizzle, sm_100 version bits
@@ -155,12 +226,14 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& b, in
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                const __grid_constant__ TcParams p) {
   if (p.skip && *p.skip) return;   // skipped loss-scaled step
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  unsigned char* epi = smem + STAGES * STAGE_BYTES;      // 4 x EPI_BYTES staging
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi + 4 * EPI_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -250,71 +323,75 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
   } else {
-    // epilogue warps 2..5: TMEM lane quarter q = warp % 4
+    // epilogue warps 2..5: TMEM lane quarter q = warp % 4, 32 rows each
     const int q = warp & 3;
-    uint32_t tl = 0;
+    const uint32_t slot = smem_u32(epi + q * EPI_BYTES);
+    // staging bytes of one 32-column chunk; the slot holds EPI_BYTES / that
+    // many chunks in flight
+    const int cbytes = (p.d_f32 ? 4096 : 2048) * (p.sym ? 2 : 1) * (p.has_d2 ? 2 : 1);
+    const int nbuf = EPI_BYTES / cbytes;
+    uint32_t ck = 0, tl = 0;
     for (int t = blockIdx.x; t < p.total_tiles && !*abort_flag; t += gridDim.x, ++tl) {
       int b, I, J;
       tile_coords(p, t, b, I, J);
       const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
       if (!mbar_wait(&tfull[acc], aph)) { fail(); break; }
       tc_fence_after();
-      const int row = I * BM + q * 32 + lane;
-      const size_t boff = (size_t)b * p.stride;
-      const __half* Cb = p.C ? reinterpret_cast<const __half*>(reinterpret_cast<const char*>(p.C) + boff)
-                             : nullptr;
-      char* Db = reinterpret_cast<char*>(p.D) + boff;
+      const int row0 = I * BM + q * 32;
+      const int row = row0 + lane;
       #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         const int col0 = J * BN + c * 32;
-        float v[32];
-        tm_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, v);
         if (col0 >= p.N) continue;
         const int cblk = col0 / 128;
         if (p.sym && cblk < I) continue;  // lower block: written as a mirror by its owner
-        if (Cb && p.beta != 0.f) {
-          const uint4* cp = reinterpret_cast<const uint4*>(Cb + (size_t)row * p.N + col0);
-          #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 u = cp[j];
-            const __half2* h = reinterpret_cast<const __half2*>(&u);
-            #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(h[e]);
-              v[8 * j + 2 * e] = fmaf(p.alpha, v[8 * j + 2 * e], p.beta * f.x);
-              v[8 * j + 2 * e + 1] = fmaf(p.alpha, v[8 * j + 2 * e + 1], p.beta * f.y);
-            }
-          }
-        } else {
-          #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
+        const bool mirror = p.sym && cblk > I;
+        float v[32], v2[32];
+        tm_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, v);
+        const bool dg = row >= col0 && row < col0 + 32;   // the diagonal crosses this row
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float d = (dg && col0 + j == row) ? 1.f : 0.f;
+          v2[j] = fmaf(p.alpha2, v[j], d * p.diag2);
+          v[j] = fmaf(p.alpha, v[j], d * p.diag);
         }
+        // the staging buffer of this chunk is free once the stores issued from
+        // it nbuf chunks ago have read it
+        if (lane == 0) bulk_wait_read(nbuf - 1);
+        __syncwarp();
+        const uint32_t buf = slot + (ck % nbuf) * cbytes;
         if (p.d_f32) {
-          float4* dp = reinterpret_cast<float4*>(reinterpret_cast<float*>(Db) + (size_t)row * p.N + col0);
-          #pragma unroll
-          for (int j = 0; j < 8; ++j) dp[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          stage_row_f(buf, lane, v);
         } else {
-          __half* D = reinterpret_cast<__half*>(Db);
-          uint4* dp = reinterpret_cast<uint4*>(D + (size_t)row * p.N + col0);
-          #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 u;
-            __half2* h = reinterpret_cast<__half2*>(&u);
-            #pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
-            dp[j] = u;
-          }
-          if (p.sym && cblk > I) {
-            // mirror: D[col][row]; lanes hold consecutive rows -> coalesced
-            #pragma unroll
-            for (int j = 0; j < 32; ++j) D[(size_t)(col0 + j) * p.N + row] = __float2half_rn(v[j]);
+          stage_row_h(buf, lane, v);
+          if (mirror) stage_col_h(buf + 2048, lane, v);
+          if (p.has_d2) {
+            const uint32_t b2 = buf + (p.sym ? 4096 : 2048);
+            stage_row_h(b2, lane, v2);
+            if (mirror) stage_col_h(b2 + 2048, lane, v2);
           }
         }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmD, buf, col0, row0, b);
+          if (mirror) tma_store_3d(&tmD, buf + 2048, row0, col0, b);
+          if (p.has_d2) {
+            const uint32_t b2 = buf + (p.sym ? 4096 : 2048);
+            tma_store_3d(&tmD2, b2, col0, row0, b);
+            if (mirror) tma_store_3d(&tmD2, b2 + 2048, row0, col0, b);
+          }
+          bulk_commit();
+        }
+        ++ck;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
+    // every store has left shared memory and reached global memory
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -337,16 +414,21 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
+// 3-D tensor map [batch][outer][inner]: MMA operands (fp16, 128-byte swizzle)
+// and epilogue outputs (32 x 32 boxes: fp16 with the 64-byte swizzle, fp32
+// with the 128-byte swizzle, matching the staging tiles)
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t batch,
-              uint64_t row_bytes, uint64_t batch_bytes, uint32_t box_inner, uint32_t box_outer) {
+              uint64_t row_bytes, uint64_t batch_bytes, uint32_t box_inner, uint32_t box_outer,
+              bool f32 = false, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = get_encode();
   if (!enc) return false;
   const cuuint64_t dims[3] = {inner, outer, batch};
   const cuuint64_t strides[2] = {row_bytes, batch_bytes};
   const cuuint32_t box[3] = {box_inner, box_outer, 1};
   const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -374,7 +456,7 @@ uint32_t tc_idesc_f16(int m, int n, int b_mn) {
   return d;
 }
 
-size_t tc_gemm_smem_bytes() { return STAGES * STAGE_BYTES + 1024 + 256; }
+size_t tc_gemm_smem_bytes() { return STAGES * STAGE_BYTES + 4 * EPI_BYTES + 1024 + 256; }
 
 cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
   if (g.M % BM || g.N % 128 || g.K % BK || g.batch < 1 || (g.sym && g.M != g.N))
@@ -389,6 +471,19 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
       : make_map(&tb, g.B, (uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.batch, (uint64_t)g.K * 2, g.stride,
                  BK, BN);
   if (!ok_b) return cudaErrorInvalidValue;
+  if (g.d_f32 && (g.sym || g.D2)) return cudaErrorInvalidValue;   // mirrors and D2 are fp16
+  CUtensorMap td, td2;
+  if (!make_map(&td, g.D, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.batch,
+                (uint64_t)g.N * (g.d_f32 ? 4 : 2), g.stride, 32, 32, g.d_f32 != 0,
+                g.d_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  if (g.D2) {
+    if (!make_map(&td2, g.D2, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.batch, (uint64_t)g.N * 2,
+                  g.stride, 32, 32, false, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  } else {
+    td2 = td;
+  }
   TcParams p;
   p.M = (int)g.M; p.N = (int)g.N; p.K = (int)g.K;
   p.tiles_m = (int)(g.M / BM);
@@ -401,11 +496,10 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
     p.tiles_per_batch = p.tiles_m * p.tiles_n;
   }
   p.total_tiles = p.tiles_per_batch * g.batch;
-  p.stride = g.stride;
-  p.C = static_cast<const __half*>(g.C);
-  p.D = g.D;
   p.d_f32 = g.d_f32;
-  p.alpha = g.alpha; p.beta = g.beta;
+  p.has_d2 = g.D2 ? 1 : 0;
+  p.alpha = g.alpha; p.diag = g.diag;
+  p.alpha2 = g.alpha2; p.diag2 = g.diag2;
   p.sym = g.sym; p.b_mn = g.b_mn;
   p.idesc = tc_idesc_f16(BM, BN, g.b_mn);
   p.err = g.err;
@@ -415,7 +509,7 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
                                        (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
-  tc_gemm_kernel<<<grid, NTHREADS, smem, s>>>(ta, tb, p);
+  tc_gemm_kernel<<<grid, NTHREADS, smem, s>>>(ta, tb, td, td2, p);
   return cudaGetLastError();
 }
 
