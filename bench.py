@@ -346,22 +346,37 @@ def run_ours(args, w):
     ms = max_over_ranks(sum(per) / len(per), dev)
     err = mu.workspace_error(wsp, stream)
 
-    # ---- end to end through the public API, host buffers (pinned)
-    Wh = [x.cpu().pin_memory() for x in W]
-    Gh = [x.cpu().pin_memory() for x in G]
-    Mh = [x.cpu().pin_memory() for x in M]
-    h2d = sum(x.numel() * x.element_size() for x in Wh + Gh + Mh)
-    d2h = sum(x.numel() * x.element_size() for x in Wh + Mh)
-    Wd = [torch.empty_like(x, device=dev) for x in Wh]
-    Gd = [torch.empty_like(x, device=dev) for x in Gh]
-    Md = [torch.empty_like(x, device=dev) for x in Mh]
+    # ---- end to end through the public API, host buffers (pinned).  Each
+    # kind of state (parameters, gradients, momentum) lives in one flat
+    # buffer on either side, the parameters being views into it (the layout
+    # of a flat-parameter data-parallel trainer), so a step moves it with one
+    # copy per kind and direction.
+    def flat(ts, device, pin=False):
+        buf = torch.empty(sum(x.numel() for x in ts), dtype=ts[0].dtype, device=device,
+                          pin_memory=pin)
+        views, off = [], 0
+        for x in ts:
+            views.append(buf[off:off + x.numel()].view(x.shape))
+            off += x.numel()
+        return buf, views
+
+    hW, Wh = flat(W, "cpu", True)
+    hG, Gh = flat(G, "cpu", True)
+    hM, Mh = flat(M, "cpu", True)
+    for d, h in zip(W + G + M, Wh + Gh + Mh):
+        h.copy_(d)
+    dW, Wd = flat(W, dev)
+    dG, Gd = flat(G, dev)
+    dM, Md = flat(M, dev)
+    h2d = sum(x.numel() * x.element_size() for x in (hW, hG, hM))
+    d2h = sum(x.numel() * x.element_size() for x in (hW, hM))
     opt_step = mu.PreparedStep(plan, Wd, Gd, Md, workspace=wsp, stream=stream, **hp)
 
     def e2e_step():
-        for d, h in zip(Wd + Gd + Md, Wh + Gh + Mh):
+        for d, h in ((dW, hW), (dG, hG), (dM, hM)):
             d.copy_(h, non_blocking=True)
         opt_step()
-        for d, h in zip(Wd + Md, Wh + Mh):
+        for d, h in ((dW, hW), (dM, hM)):
             h.copy_(d, non_blocking=True)
 
     for _ in range(min(args.warmup, 3)):
