@@ -613,9 +613,14 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red[warp] = ss;
   tm_wait_st();
-  // the parameter rows of pass 2 start streaming while the reductions and
-  // the m x m recursion run
-  if (staged) {
+  // The parameter rows of pass 2 start streaming while the reductions and
+  // the m x m recursion run.  When the recursion leaves warps idle, those
+  // warps issue the copies during it (issuing a bulk copy takes tens of
+  // cycles, which would otherwise delay the reductions).
+  constexpr int NB2 = MatTile<MP, NT>::NB * MatTile<MP, NT>::NB;
+  constexpr int RT = 2 * NB2 <= NT ? (2 * NB2 + 31) / 32 * 32 : NT;   // threads of the recursion
+  constexpr bool SPLIT = staged && RT < NT;
+  if (staged && !SPLIT) {
     const int ns0 = min(NSTW, nstage), parts = NW / NSTW;
     if (warp / parts < ns0) issue_stage(warp / parts, 1, warp % parts, parts);
   }
@@ -646,25 +651,39 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   __syncthreads();
 
   // ---- m x m recursion: P_t = aI + bA_t + cA_t^2;  Q <- P_t Q;  A <- P_t A_t P_t ----
-  constexpr int NB2 = MatTile<MP, NT>::NB * MatTile<MP, NT>::NB;
-  for (int t = 0; t < st.T; ++t) {
-    mat_mul<MP, NT, 1>(mP, mA, mA, tid, st.a, st.b, st.c);   // P = aI + bA + cA^2
-    __syncthreads();
-    // Q <- P Q and P A on disjoint thread sets when both fit
-    if (2 * NB2 <= NT) {
-      if (tid < NB2) mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
-      else if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid - NB2);
-    } else {
-      mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
-      if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid);
+  // The first RT threads run it, synchronised by a named barrier of their own
+  // when that leaves warps over; those issue the parameter-row copies.
+  auto rsync = [&]() {
+    if constexpr (SPLIT) asm volatile("bar.sync 1, %0;\n" ::"n"(RT) : "memory");
+    else __syncthreads();
+  };
+  if (!SPLIT || tid < RT) {
+    for (int t = 0; t < st.T; ++t) {
+      mat_mul<MP, NT, 1>(mP, mA, mA, tid, st.a, st.b, st.c);   // P = aI + bA + cA^2
+      rsync();
+      // Q <- P Q and P A on disjoint thread sets when both fit
+      if (2 * NB2 <= NT) {
+        if (tid < NB2) mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
+        else if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid - NB2);
+      } else {
+        mat_mul<MP, NT, 0>(mT1, mP, mQ, tid);
+        if (t + 1 < st.T) mat_mul<MP, NT, 0>(mT2, mP, mA, tid);
+      }
+      rsync();
+      { float* x = mQ; mQ = mT1; mT1 = x; }
+      if (t + 1 < st.T) {
+        mat_mul<MP, NT, 0>(mA, mT2, mP, tid);                    // A <- (P A) P
+        rsync();
+      }
     }
-    __syncthreads();
-    { float* x = mQ; mQ = mT1; mT1 = x; }
-    if (t + 1 < st.T) {
-      mat_mul<MP, NT, 0>(mA, mT2, mP, tid);                    // A <- (P A) P
-      __syncthreads();
-    }
+  } else {
+    // one stage per idle warp, round robin
+    constexpr int IW = (NT - RT) / 32;
+    const int ns0 = min(NSTW, nstage);
+    for (int k = warp - RT / 32; k < ns0; k += IW) issue_stage(k, 1);
+    for (int t = 0; t < st.T; ++t) { float* x = mQ; mQ = mT1; mT1 = x; }
   }
+  if constexpr (SPLIT) __syncthreads();
   // O = Q X_0 = (Q * inv) V; the bf16 A operand is the scaled Q
   const float qscale = tot > 0.f ? inv : 0.f;
   for (int e = tid; e < MP * MP; e += NT) {
