@@ -485,6 +485,11 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   }
   for (int q = 0; q < LOOKAHEAD; ++q) prefetch_sc(q);
 
+  // threads of the m x m recursion; SPLIT: the remaining warps are idle then
+  constexpr int NB2 = MatTile<MP, NT>::NB * MatTile<MP, NT>::NB;
+  constexpr int RT = 2 * NB2 <= NT ? (2 * NB2 + 31) / 32 * 32 : NT;
+  constexpr bool SPLIT = staged && RT < NT;
+
   // ---- pass 1: momentum, V (bf16 in TMEM), sum of squares, Gram of V ----------
   float ss = 0.f;
   float gacc[NP][MB][4];
@@ -574,10 +579,12 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     gram_accum<MB>(gacc, xr);
   }
 
-  // warm L2 with this CTA's parameter rows for the final update
-  if (warp == NW - 1 && jc1 > jc0) {
+  // warm L2 with this CTA's parameter rows for the final update, columns
+  // [c0, end of the CTA's range); one warp
+  auto prefetch_w_l2 = [&](int c0) {
     const size_t es = sizeof(PT);
-    const int c0 = jc0 * 32, c1 = min(p.n, jc1 * 32);
+    const int c1 = min(p.n, jc1 * 32);
+    if (c1 <= c0) return;
     const int rows = p.tr ? 1 : p.m;
     for (int i = lane; i < rows; i += 32) {
       const char* a = reinterpret_cast<const char*>(W) +
@@ -590,7 +597,9 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
                      "r"((uint32_t)(s1 - s0))
                      : "memory");
     }
-  }
+  };
+  // (with idle warps during the recursion, they warm it there instead)
+  if (!SPLIT && warp == NW - 1 && jc1 > jc0) prefetch_w_l2(jc0 * 32);
 
   // ---- cluster-wide ||V||^2 and V V^T (fixed order: warps, then ranks) -----------
   __syncthreads();   // every pass-1 stage is consumed: the ring takes W rows
@@ -617,9 +626,6 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   // the m x m recursion run.  When the recursion leaves warps idle, those
   // warps issue the copies during it (issuing a bulk copy takes tens of
   // cycles, which would otherwise delay the reductions).
-  constexpr int NB2 = MatTile<MP, NT>::NB * MatTile<MP, NT>::NB;
-  constexpr int RT = 2 * NB2 <= NT ? (2 * NB2 + 31) / 32 * 32 : NT;   // threads of the recursion
-  constexpr bool SPLIT = staged && RT < NT;
   if (staged && !SPLIT) {
     const int ns0 = min(NSTW, nstage), parts = NW / NSTW;
     if (warp / parts < ns0) issue_stage(warp / parts, 1, warp % parts, parts);
@@ -677,10 +683,12 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
       }
     }
   } else {
-    // one stage per idle warp, round robin
+    // one stage per idle warp, round robin; the last idle warp then warms L2
+    // with the columns the ring does not hold yet
     constexpr int IW = (NT - RT) / 32;
     const int ns0 = min(NSTW, nstage);
     for (int k = warp - RT / 32; k < ns0; k += IW) issue_stage(k, 1);
+    if (warp == NW - 1) prefetch_w_l2(c_lo + ns0 * S::SW);
     for (int t = 0; t < st.T; ++t) { float* x = mQ; mQ = mT1; mT1 = x; }
   }
   if constexpr (SPLIT) __syncthreads();
