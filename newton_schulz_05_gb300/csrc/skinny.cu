@@ -212,7 +212,9 @@ struct SkinnySmem {
   static constexpr int NP = (MB + 1) / 2;
   static constexpr int MPX = 16 * NP;
   static constexpr size_t MAT = sizeof(float) * MP * MP;             // Gram partials
-  static constexpr int LDM = MP + 1;                                   // padded row of the
+  // padded row of the m x m matrices: odd for distinct banks of column
+  // reads, even for 8-byte row reads (the 2 x 2 register tiles, m <= 32)
+  static constexpr int LDM = MB <= 4 ? MP + 2 : MP + 1;
   static constexpr size_t MATP = sizeof(float) * MP * LDM;             // m x m matrices
   // for m > 32 the five m x m matrices reuse the warp-partial region, dead
   // once the CTA partial is formed (NW = 8 >= 5); no ring is used there
@@ -302,13 +304,18 @@ struct MatTile {
 
 // D[i][j] = sum_k A[i][k] B[k][j]  (+ fused P epilogue when MODE == 1:
 // D = c*(A A) + b*A + a*I, with B == A), MP x MP fp32 in shared memory with
-// rows MP + 1 floats apart.
+// rows LDM floats apart (LDM = MP + 2 for the 2 x 2 tiles, else MP + 1).
+//
+// Every left operand of the recursion is symmetric in exact arithmetic (A_t,
+// P_t and P_t A_t are polynomials in A_0), so with 2 x 2 tiles its column
+// k is read as row k: both operands then come in 8-byte row reads.  The
+// transposed read differs from the direct one by fp32 rounding only.
 template <int MP, int NT, int MODE>
 __device__ __forceinline__ void mat_mul(float* D, const float* A, const float* B, int tid,
                                         float a = 0.f, float b = 0.f, float c = 0.f) {
-  constexpr int LDM = MP + 1;   // padded rows: the A-operand reads of a warp hit distinct banks
   using T = MatTile<MP, NT>;
   constexpr int TB = T::TB, NB = T::NB;
+  constexpr int LDM = TB == 2 ? MP + 2 : MP + 1;
   if (tid >= NB * NB) return;
   const int i0 = (tid / NB) * TB, j0 = (tid % NB) * TB;
   float acc[TB][TB];
@@ -321,10 +328,17 @@ __device__ __forceinline__ void mat_mul(float* D, const float* A, const float* B
   #pragma unroll
   for (int k = 0; k < MP; ++k) {
     float av[TB], bv[TB];
-    #pragma unroll
-    for (int x = 0; x < TB; ++x) av[x] = (i0 + x < MP) ? A[(i0 + x) * LDM + k] : 0.f;
-    #pragma unroll
-    for (int y = 0; y < TB; ++y) bv[y] = (j0 + y < MP) ? B[k * LDM + j0 + y] : 0.f;
+    if constexpr (TB == 2) {
+      // MP is a multiple of 8 and i0, j0 are even: both pairs exist
+      const float2 ap = *reinterpret_cast<const float2*>(A + k * LDM + i0);
+      const float2 bp = *reinterpret_cast<const float2*>(B + k * LDM + j0);
+      av[0] = ap.x; av[1] = ap.y; bv[0] = bp.x; bv[1] = bp.y;
+    } else {
+      #pragma unroll
+      for (int x = 0; x < TB; ++x) av[x] = (i0 + x < MP) ? A[(i0 + x) * LDM + k] : 0.f;
+      #pragma unroll
+      for (int y = 0; y < TB; ++y) bv[y] = (j0 + y < MP) ? B[k * LDM + j0 + y] : 0.f;
+    }
     #pragma unroll
     for (int x = 0; x < TB; ++x)
       #pragma unroll
@@ -485,6 +499,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   }
   for (int q = 0; q < LOOKAHEAD; ++q) prefetch_sc(q);
 
+  static_assert(S::LDM == (MatTile<MP, NT>::TB == 2 ? MP + 2 : MP + 1), "m x m row pitch");
   // threads of the m x m recursion; SPLIT: the remaining warps are idle then
   constexpr int NB2 = MatTile<MP, NT>::NB * MatTile<MP, NT>::NB;
   constexpr int RT = 2 * NB2 <= NT ? (2 * NB2 + 31) / 32 * 32 : NT;
@@ -651,8 +666,8 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     const int src = gram_covered(i, j) ? e : j * MP + i;
     float s = 0.f;
     for (int r = 0; r < p.cluster; ++r) s += cluster.map_shared_rank(gram_c, r)[src];
-    mA[i * (MP + 1) + j] = s * inv * inv;         // A_0 = X_0 X_0^T
-    mQ[i * (MP + 1) + j] = i == j ? 1.f : 0.f;
+    mA[i * S::LDM + j] = s * inv * inv;           // A_0 = X_0 X_0^T
+    mQ[i * S::LDM + j] = i == j ? 1.f : 0.f;
   }
   __syncthreads();
 
@@ -696,7 +711,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   const float qscale = tot > 0.f ? inv : 0.f;
   for (int e = tid; e < MP * MP; e += NT) {
     const int i = e / MP, j = e % MP;
-    qh[i * MPX + j] = __float2bfloat16_rn(mQ[i * (MP + 1) + j] * qscale);
+    qh[i * MPX + j] = __float2bfloat16_rn(mQ[i * S::LDM + j] * qscale);
   }
   __syncthreads();
   uint32_t afr[NP][NP][4];
