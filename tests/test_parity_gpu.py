@@ -26,8 +26,12 @@ def test_fp32_single_matrix_24x1024_both_modes():
         run_and_check([(24, 1024)], torch.float32, HP, mode=mode, grad_std=1.0)
 
 
+# m covers every row-block count of the fused kernel (1, 2, 3, 4, 6, 8 blocks
+# of 8 rows), with n a multiple of 8 (rows streamed through the shared-memory
+# ring) and not (direct loads), and both orientations
 SKINNY = [(24, 1024), (24, 10240), (5, 77), (64, 300), (20, 33), (1, 1), (1, 500), (500, 1),
-          (8, 8), (40, 2000), (56, 130), (1000, 24), (300, 64), (17, 4099), (3, 24, 500)]
+          (8, 8), (40, 2000), (56, 130), (1000, 24), (300, 64), (17, 4099), (3, 24, 500),
+          (12, 3000), (16, 520), (32, 2048), (30, 1000), (2000, 12)]
 
 
 @pytest.mark.parametrize("shape", SKINNY, ids=lambda s: "x".join(map(str, s)))
