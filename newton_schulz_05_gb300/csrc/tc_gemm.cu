@@ -52,7 +52,8 @@ struct TcParams {
   float alpha2, diag2; // D2 = alpha2 * acc + diag2 * I
   int sym;
   int b_mn;
-  uint32_t idesc;
+  uint32_t idesc;      // M = 128, N = 256
+  uint32_t idesc128;   // M = 128, N = 128: tiles with one 128-column half to compute
   int* err;
   const int* skip;
 };
@@ -297,10 +298,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       uint32_t it = 0, tl = 0;
       for (int t = blockIdx.x; t < p.total_tiles && !*abort_flag; t += gridDim.x, ++tl) {
+        int b, I, J;
+        tile_coords(p, t, b, I, J);
+        // a 128-column half of the tile that no epilogue stores is not
+        // computed: past N, or (symmetric) the block left of the diagonal
+        const int n_lo = (p.sym && 2 * J < I) ? 128 : 0;
+        const int n_hi = J * BN + BN > p.N ? p.N - J * BN : BN;
+        const uint32_t idesc = n_hi - n_lo == BN ? p.idesc : p.idesc128;
         const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1)) { fail(); break; }
         tc_fence_after();
-        const uint32_t dt = tmem + acc * BN;
+        const uint32_t dt = tmem + acc * BN + n_lo;
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % STAGES;
@@ -308,13 +316,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (!mbar_wait(&full[s], ph)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
+          // K-major B: row n_lo of the tile starts n_lo * 128 bytes in (a
+          // whole number of 1024-byte swizzle atoms); N-major B has n_lo = 0
+          const uint32_t sb = sa + A_BYTES + n_lo * (BK * 2);
           #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = sdesc(sa + k * 32, 16, 1024);
             const uint64_t bd = p.b_mn ? sdesc(sb + k * 2048, 64 * BK * 2, 1024)
                                        : sdesc(sb + k * 32, 16, 1024);
-            mma_f16(dt, ad, bd, p.idesc, (kb | k) != 0);
+            mma_f16(dt, ad, bd, idesc, (kb | k) != 0);
           }
           mma_commit(&empty[s]);
         }
@@ -502,6 +512,7 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
   p.alpha2 = g.alpha2; p.diag2 = g.diag2;
   p.sym = g.sym; p.b_mn = g.b_mn;
   p.idesc = tc_idesc_f16(BM, BN, g.b_mn);
+  p.idesc128 = tc_idesc_f16(BM, 128, g.b_mn);
   p.err = g.err;
   p.skip = g.skip;
   const size_t smem = tc_gemm_smem_bytes();
