@@ -24,6 +24,7 @@ max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -457,10 +458,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="skinny_74x24x10240", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ns-steps", type=int, default=None,
+                    help="Newton-Schulz steps T (default: the workload's, 5); T = 0 times "
+                         "the step without the iteration, for its share of the step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = synth.workload(args.workload)
+    if args.ns_steps is not None:
+        w = dataclasses.replace(w, ns_steps=args.ns_steps)
     if args.impl == "reference":
         run_reference(args, w)
     else:
