@@ -707,8 +707,12 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     for (int t = 0; t < st.T; ++t) { float* x = mQ; mQ = mT1; mT1 = x; }
   }
   if constexpr (SPLIT) __syncthreads();
-  // O = Q X_0 = (Q * inv) V; the bf16 A operand is the scaled Q
-  const float qscale = tot > 0.f ? inv : 0.f;
+  // O = Q X_0 = (Q * inv) V; the bf16 A operand is the scaled Q.  When O is
+  // not an output, the update's factor -lr s is folded in too, so that the
+  // product is the update term itself: W' = W (1 - lr wd) + (-lr s inv Q) V
+  // (ring-staged path)
+  const bool fold = staged && Oout == nullptr;
+  const float qscale = tot > 0.f ? (fold ? -p.lrs * inv : inv) : 0.f;
   for (int e = tid; e < MP * MP; e += NT) {
     const int i = e / MP, j = e % MP;
     qh[i * MPX + j] = __float2bfloat16_rn(mQ[i * S::LDM + j] * qscale);
@@ -819,6 +823,32 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
       }
     }
     const int cb = sc_col(q);
+    if (fold) {
+      // o holds -lr s O: one multiply-add per parameter
+      #pragma unroll
+      for (int rb = 0; rb < MB; ++rb)
+        #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = cb + h * 16 + 4 * t4;
+          if (row_ok(rb) && c < p.n) {
+            float wn[4];
+            wn[0] = fmaf(wcur[rb][h][0], p.decay, o[rb][2 * h][0]);
+            wn[1] = fmaf(wcur[rb][h][1], p.decay, o[rb][2 * h][1]);
+            wn[2] = fmaf(wcur[rb][h][2], p.decay, o[rb][2 * h + 1][0]);
+            wn[3] = fmaf(wcur[rb][h][3], p.decay, o[rb][2 * h + 1][1]);
+            PT* wp = W + (mo_row[rb] - Mo) + c;     // same row offset as the momentum
+            if constexpr (sizeof(PT) == 2) {
+              uint2 u;
+              u.x = pack_bf16(wn[0], wn[1]);
+              u.y = pack_bf16(wn[2], wn[3]);
+              *reinterpret_cast<uint2*>(wp) = u;
+            } else {
+              *reinterpret_cast<float4*>(wp) = make_float4(wn[0], wn[1], wn[2], wn[3]);
+            }
+          }
+        }
+      continue;
+    }
     #pragma unroll
     for (int rb = 0; rb < MB; ++rb)
       #pragma unroll

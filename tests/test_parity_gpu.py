@@ -189,3 +189,41 @@ def test_nan_gradient_propagates():
         Wd = [W[0].cuda()]
         gpu_step(plan, Wd, [G.cuda()], [M[0].cuda()], HP, ortho=False)
         assert torch.isnan(Wd[0]).any()
+
+
+@pytest.mark.parametrize("shape", [(24, 10240), (12, 3000), (16, 520), (32, 2048), (2, 24, 1024)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_step_without_O_output(shape, dtype):
+    """When O is not requested, the fused kernel folds -lr s into Q and applies
+    the update as one multiply-add: its W' must agree with the oracle (the O
+    tolerance carried through lr s, plus the rounding of W') and with the
+    step that also writes O (which differs only by the bf16 rounding of the
+    differently scaled Q); the momentum is the same bits."""
+    m = muon()
+    W, Gs, M = make_inputs([shape], dtype)
+    plan = m.Plan([(shape, dtype)])
+    assert plan.groups()[0]["kernel"] == m.KERNEL_SKINNY
+    W1, M1 = [W[0].cuda()], [M[0].cuda()]
+    O = gpu_step(plan, W1, [Gs[0][0].cuda()], M1, HP)
+    W2, M2 = [W[0].cuda()], [M[0].cuda()]
+    gpu_step(plan, W2, [Gs[0][0].cuda()], M2, HP, ortho=False)
+    assert torch.equal(M1[0], M2[0])
+    ref = oracle_step(W, Gs[0], M, HP)
+    for e, (Wg1, Wg2, Og) in enumerate(zip(slices(W1[0]), slices(W2[0]), slices(O[0]))):
+        Wr, _, Or = ref[(0, e)]
+        Mr_, Nr_ = Wr.shape
+        lrs = HP["lr"] * float(np.float32(np.sqrt(max(1.0, Mr_ / Nr_))))
+        wf = Wg2.double().cpu().numpy()
+        wu = Wg1.double().cpu().numpy()
+        og = Og.double().cpu().numpy()
+        if dtype == torch.bfloat16:
+            from helpers import bf16_ulp
+            ulp = np.linalg.norm(bf16_ulp(Wr))
+        else:
+            ulp = np.linalg.norm(np.spacing(np.abs(Wr).astype(np.float32)).astype(np.float64))
+        # against the oracle
+        assert np.linalg.norm(wf - Wr) <= ulp + lrs * TOL["tc16"] * np.linalg.norm(Or), e
+        # against the step that writes O: bf16 rounding of Q (2^-8 relative per
+        # entry, 2^-6 allowed for sums of terms of both signs)
+        assert np.linalg.norm(wf - wu) <= ulp + lrs * 2.0 ** -6 * np.linalg.norm(og), e
