@@ -243,3 +243,15 @@ def test_partition_rejects_bad_arguments(muon):
     assert L.muon_plan_partition(plan.handle, 2, 5, 1e15, 1e12, None, None) == -1
     assert L.muon_plan_partition(None, 2, 5, 1e15, 1e12, own, None) == -1
     assert L.muon_plan_partition(plan.handle, 3, 5, 1e15, 1e12, own, None) == 0 and own[0] == 0
+
+
+def test_partition_with_more_replicas_than_slices(muon):
+    import torch
+    plan = muon.Plan([((24, 64), torch.bfloat16), ((2, 100, 80), torch.float32)])
+    owner, load = plan.partition(8)
+    assert len(owner) == 3 and sorted(owner) == [0, 1, 2]
+    assert load[3:] == [0.0] * 5 and all(x > 0 for x in load[:3])
+    o_owner, o_load = _oracle_partition(plan, 8, 5, muon.GB300_FLOPS, muon.GB300_HBM_BYTES)
+    assert owner == o_owner and load == o_load
+    part = muon.Partition(plan, 8)
+    assert part.owned(7) == [] and part.owned(0) != []
