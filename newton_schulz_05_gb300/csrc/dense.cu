@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kNT) front_kernel(
     const __grid_constant__ SlicePtrs ptrs, int64_t m, int64_t n, int64_t m_pad,
     int64_t n_pad, int tr, int vec, float beta, int nesterov, float gscale, const int* skip,
     char* ws, size_t slice_ws, size_t off_V, size_t off_part) {
+  pdl_wait();
   if (skip && *skip) return;   // skipped loss-scaled step: momentum untouched
   const int s = blockIdx.y;
   const int tiles_c = (int)(n_pad / kFrontTileC);
@@ -148,6 +149,7 @@ __global__ void __launch_bounds__(kNT) front_kernel(
 __global__ void __launch_bounds__(kNT) finalize_kernel(char* ws, size_t slice_ws,
                                                        size_t off_part, size_t off_inv,
                                                        int nblk, float eps) {
+  pdl_wait();
   char* base = ws + (size_t)blockIdx.x * slice_ws;
   const float* part = reinterpret_cast<const float*>(base + off_part);
   __shared__ float red[kNT / 32];
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(kNT) normalize_kernel(char* ws, size_t slice_w
                                                         size_t off_V, size_t off_X,
                                                         size_t off_inv, int64_t count,
                                                         int in_place) {
+  pdl_wait();
   char* base = ws + (size_t)blockIdx.y * slice_ws;
   float* V = reinterpret_cast<float*>(base + off_V);
   IT* X = reinterpret_cast<IT*>(base + off_X);
@@ -191,6 +194,7 @@ template <typename PT>
 __global__ void __launch_bounds__(kNT) epilogue_kernel(
     const __grid_constant__ SlicePtrs ptrs, int64_t M, int64_t N, int64_t n_pad, int tr, int vec,
     float decay, float lr_scale, const int* skip, char* ws, size_t slice_ws, size_t off_O) {
+  pdl_wait();
   if (skip && *skip) return;   // skipped loss-scaled step: parameters untouched
   const int s = blockIdx.y;
   const float* O = reinterpret_cast<const float*>(ws + (size_t)s * slice_ws + off_O);
@@ -263,7 +267,7 @@ Offsets dense_offsets(const Group& g, int mode) {
 
 template <typename IT>
 cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
-                      const StepArgs& st, char* ws, int* err_word, cudaStream_t s) {
+                      const StepArgs& st, char* ws, int* err_word, cudaStream_t s, bool pdl_first) {
   const Offsets off = dense_offsets(g, mode);
   const size_t sws = g.slice_ws;
   const int64_t mp = g.m_pad, np = g.n_pad;
@@ -277,20 +281,27 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
     if (a % (4 * es) || reinterpret_cast<uintptr_t>(ptrs.Mom[i]) % 16) vec = 0;
     if (ptrs.O[i] && reinterpret_cast<uintptr_t>(ptrs.O[i]) % 16) vec = 0;
   }
+  // every launch after the step's first may overlap the previous kernel's
+  // tail (programmatic dependent launch; each kernel waits before reading)
+  cudaError_t le;
   if (g.dtype == MUON_BF16)
-    front_kernel<__nv_bfloat16><<<fgrid, kNT, 0, s>>>(ptrs, g.m, g.n, mp, np, g.tr, vec, st.beta,
-                                                      st.nesterov, st.gscale, st.skip, ws, sws,
-                                                      off.V, off.part);
+    le = launch_k(front_kernel<__nv_bfloat16>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m, g.n,
+                  mp, np, (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip, ws, sws, off.V,
+                  off.part);
   else
-    front_kernel<float><<<fgrid, kNT, 0, s>>>(ptrs, g.m, g.n, mp, np, g.tr, vec, st.beta,
-                                              st.nesterov, st.gscale, st.skip, ws, sws, off.V,
-                                              off.part);
-  finalize_kernel<<<ns, kNT, 0, s>>>(ws, sws, off.part, off.inv, nblk, st.eps);
+    le = launch_k(front_kernel<float>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m, g.n, mp, np,
+                  (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip, ws, sws, off.V,
+                  off.part);
+  if (le != cudaSuccess) return le;
+  le = launch_k(finalize_kernel, dim3(ns), dim3(kNT), 0, s, true, ws, sws, off.part, off.inv, nblk,
+                st.eps);
+  if (le != cudaSuccess) return le;
   const int64_t cnt = mp * np;
   int nb = (int)((cnt / 4 + kNT - 1) / kNT);
   if (nb > 1184) nb = 1184;
-  normalize_kernel<IT><<<dim3(nb, ns), kNT, 0, s>>>(ws, sws, off.V, off.X0, off.inv, cnt,
-                                                     st.T == 0 ? 1 : 0);
+  le = launch_k(normalize_kernel<IT>, dim3(nb, ns), dim3(kNT), 0, s, true, ws, sws, off.V, off.X0,
+                off.inv, cnt, st.T == 0 ? 1 : 0);
+  if (le != cudaSuccess) return le;
   size_t xin = off.X0, xout = off.X1;
   if constexpr (sizeof(IT) == 2) {
     // fp16 operands: the three products on the tcgen05 tensor cores.  The
@@ -363,13 +374,10 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   const float decay = 1.f - st.lr * st.wd;
   const float lrs = st.lr * g.scale;
   if (g.dtype == MUON_BF16)
-    epilogue_kernel<__nv_bfloat16><<<dim3(tiles, ns), kNT, 0, s>>>(ptrs, g.M, g.N, np, g.tr, vec,
-                                                                  decay, lrs, st.skip, ws, sws,
-                                                                  off.V);
-  else
-    epilogue_kernel<float><<<dim3(tiles, ns), kNT, 0, s>>>(ptrs, g.M, g.N, np, g.tr, vec, decay,
-                                                          lrs, st.skip, ws, sws, off.V);
-  return cudaGetLastError();
+    return launch_k(epilogue_kernel<__nv_bfloat16>, dim3(tiles, ns), dim3(kNT), 0, s, true, ptrs,
+                    g.M, g.N, np, (int)g.tr, vec, decay, lrs, st.skip, ws, sws, off.V);
+  return launch_k(epilogue_kernel<float>, dim3(tiles, ns), dim3(kNT), 0, s, true, ptrs, g.M, g.N,
+                  np, (int)g.tr, vec, decay, lrs, st.skip, ws, sws, off.V);
 }
 
 }  // namespace
@@ -423,9 +431,10 @@ cudaError_t launch_check_finite(const Group& g, const SlicePtrs& ptrs, int nslic
 
 cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& ptrs,
                                      int nslices, const StepArgs& st, char* ws,
-                                     int* err_word, cudaStream_t s) {
-  if (mode == MUON_MODE_FP32) return run_dense<float>(g, mode, ptrs, nslices, st, ws, err_word, s);
-  return run_dense<__half>(g, mode, ptrs, nslices, st, ws, err_word, s);
+                                     int* err_word, cudaStream_t s, bool pdl_first) {
+  if (mode == MUON_MODE_FP32)
+    return run_dense<float>(g, mode, ptrs, nslices, st, ws, err_word, s, pdl_first);
+  return run_dense<__half>(g, mode, ptrs, nslices, st, ws, err_word, s, pdl_first);
 }
 
 }  // namespace muon

@@ -78,9 +78,11 @@ size_t dense_slice_ws(const Group& g, int mode);
 cudaError_t launch_skinny(const Group& g, const SlicePtrs& ptrs, int nslices,
                           const StepArgs& st, int* err_word, cudaStream_t s);
 
+// pdl_first: the chunk's first kernel may overlap the previous kernel on the
+// stream (false for the first launch of a step)
 cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& ptrs,
                                      int nslices, const StepArgs& st, char* ws,
-                                     int* err_word, cudaStream_t s);
+                                     int* err_word, cudaStream_t s, bool pdl_first);
 
 int dense_launches(int ns_steps);
 

@@ -67,6 +67,8 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
         if (launch_check_finite(g, ptrs, ns, found_inf, s) != cudaSuccess) return MUON_ERR_CUDA;
       }
   }
+  // kernels after the step's first may overlap their predecessor's tail
+  bool first = found_inf == nullptr;
   for (const Group& g : P->groups) {
     const int cnt = g.count();
     const int per = g.kernel == MUON_KERNEL_SKINNY ? kMaxSlicesPerLaunch : g.chunk;
@@ -77,8 +79,9 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
       if (g.kernel == MUON_KERNEL_SKINNY)
         e = launch_skinny(g, ptrs, ns, st, err_word, s);
       else
-        e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body, err_word, s);
+        e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body, err_word, s, !first);
       if (e != cudaSuccess) return MUON_ERR_CUDA;
+      first = false;
     }
   }
   return MUON_OK;

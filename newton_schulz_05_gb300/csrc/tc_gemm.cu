@@ -229,7 +229,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                const __grid_constant__ TcParams p) {
-  if (p.skip && *p.skip) return;   // skipped loss-scaled step
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -260,13 +259,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int kblocks = p.K / BK;
+  // launched as a dependent of the previous kernel: the setup above overlaps
+  // its tail; nothing global is touched before it has completed
+  pdl_wait();
+  // a skipped loss-scaled step computes nothing
+  const bool skipped = p.skip && *p.skip;
 
   auto fail = [&]() {
     *abort_flag = 1;
     atomicExch(p.err, kDevErrTimeout);
   };
 
-  if (warp == 0) {
+  if (skipped) {
+    // no role runs; only the teardown below
+  } else if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
       for (int t = blockIdx.x; t < p.total_tiles && !*abort_flag; t += gridDim.x) {
@@ -520,8 +526,8 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
                                        (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
-  tc_gemm_kernel<<<grid, NTHREADS, smem, s>>>(ta, tb, td, td2, p);
-  return cudaGetLastError();
+  // a product always follows another kernel of the step: dependent launch
+  return launch_k(tc_gemm_kernel, dim3(grid), dim3(NTHREADS), smem, s, true, ta, tb, td, td2, p);
 }
 
 }  // namespace muon
