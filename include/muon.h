@@ -59,9 +59,11 @@ enum { MUON_BF16 = 0, MUON_F32 = 1 };
 
 /* arithmetic of the Newton-Schulz products */
 enum {
-  /* fp16 tensor-core operands, fp32 accumulation; the iterates are
-   * normalised (spectral norm <= 1.21), so fp16 cannot overflow and carries
-   * three more mantissa bits than bf16 */
+  /* 16-bit tensor-core operands, fp32 accumulation.  Dense groups iterate
+   * in fp16: the iterates are normalised (spectral norm <= 1.21), so fp16
+   * cannot overflow and carries three more mantissa bits than bf16.  The
+   * fused kernel of skinny groups keeps V in bf16 and runs the m x m
+   * recursion in fp32; its two products take bf16 operands. */
   MUON_MODE_TC16 = 0,
   /* fp32 operands and accumulation throughout (accuracy mode) */
   MUON_MODE_FP32 = 1

@@ -1,0 +1,90 @@
+/* The C ABI of libmuon used from plain C (no Python, no CUDA headers): plan a
+ * parameter set, query groups and slices, assign slices to replicas, and
+ * check the argument errors, all host-only calls.  Prints "ok" and exits 0
+ * when every check holds; otherwise prints the failed check and exits 1. */
+#include <stdio.h>
+#include <string.h>
+
+#include "muon.h"
+
+static int fails = 0;
+#define CHECK(c)                                              \
+  do {                                                        \
+    if (!(c)) {                                               \
+      printf("failed: %s (line %d)\n", #c, __LINE__);         \
+      ++fails;                                                \
+    }                                                         \
+  } while (0)
+
+int main(void) {
+  /* 74 bf16 [24,10240] matrices, an fp32 [1408,2048] stack of 3, a
+   * transposed bf16 [2048,1408] matrix */
+  muon_shape shapes[76];
+  for (int i = 0; i < 74; ++i) {
+    shapes[i].ndim = 2;
+    shapes[i].dims[0] = 24;
+    shapes[i].dims[1] = 10240;
+    shapes[i].dims[2] = 0;
+    shapes[i].dtype = MUON_BF16;
+  }
+  shapes[74].ndim = 3;
+  shapes[74].dims[0] = 3;
+  shapes[74].dims[1] = 1408;
+  shapes[74].dims[2] = 2048;
+  shapes[74].dtype = MUON_F32;
+  shapes[75].ndim = 2;
+  shapes[75].dims[0] = 2048;
+  shapes[75].dims[1] = 1408;
+  shapes[75].dims[2] = 0;
+  shapes[75].dtype = MUON_BF16;
+
+  muon_options opt;
+  muon_options_default(&opt);
+  CHECK(opt.mode == MUON_MODE_TC16 && opt.skinny_max_m == 64);
+
+  muon_plan_t* plan = NULL;
+  CHECK(muon_plan(shapes, 76, &opt, &plan) == MUON_OK && plan != NULL);
+
+  int ng = 0, ns = 0;
+  CHECK(muon_plan_num_groups(plan, &ng) == MUON_OK && ng == 3);
+  CHECK(muon_plan_num_slices(plan, &ns) == MUON_OK && ns == 78);
+  muon_group_info gi;
+  CHECK(muon_plan_group(plan, 0, &gi) == MUON_OK);
+  CHECK(gi.m == 24 && gi.n == 10240 && gi.count == 74 && gi.tr == 0 &&
+        gi.kernel == MUON_KERNEL_SKINNY && gi.cluster == 2 && gi.scale == 1.0f);
+  CHECK(muon_plan_group(plan, 2, &gi) == MUON_OK);
+  CHECK(gi.M == 2048 && gi.N == 1408 && gi.m == 1408 && gi.tr == 1 &&
+        gi.kernel == MUON_KERNEL_DENSE);
+  int g = -1, idx = -1;
+  CHECK(muon_plan_slice(plan, 74, 2, &g, &idx) == MUON_OK && g == 1 && idx == 2);
+  size_t ws = 0;
+  CHECK(muon_plan_workspace_bytes(plan, &ws) == MUON_OK && ws > 256 && ws % 256 == 0);
+  int launches = 0;
+  CHECK(muon_plan_launches(plan, 5, &launches) == MUON_OK && launches == 1 + 2 * 19);
+
+  /* replicas: every slice has one owner, the loads sum up */
+  int owner[78];
+  double load[4];
+  CHECK(muon_plan_partition(plan, 4, 5, 1.88e15, 6.78e12, owner, load) == MUON_OK);
+  int count[4] = {0, 0, 0, 0};
+  for (int s = 0; s < 78; ++s) {
+    CHECK(owner[s] >= 0 && owner[s] < 4);
+    if (owner[s] >= 0 && owner[s] < 4) ++count[owner[s]];
+  }
+  for (int r = 0; r < 4; ++r) CHECK(count[r] > 0 && load[r] > 0.0);
+
+  /* argument errors are status codes, before any device work */
+  CHECK(muon_plan(NULL, 1, NULL, &plan) == MUON_ERR_INVALID_ARG);
+  shapes[0].ndim = 1;
+  muon_plan_t* bad = NULL;
+  CHECK(muon_plan(shapes, 1, NULL, &bad) == MUON_ERR_UNSUPPORTED_SHAPE && bad == NULL);
+  CHECK(muon_step(plan, NULL, NULL, NULL, 0.02f, 0.95f, 0.1f, 1, 5, NULL, NULL, 0, NULL) ==
+        MUON_ERR_INVALID_ARG);
+  CHECK(muon_plan_partition(plan, 0, 5, 1.0, 1.0, owner, NULL) == MUON_ERR_INVALID_ARG);
+  CHECK(strcmp(muon_status_string(MUON_ERR_WORKSPACE), "workspace too small for the plan") == 0);
+
+  muon_plan_destroy(plan);
+  if (fails) return 1;
+  printf("ok\n");
+  return 0;
+}

@@ -255,3 +255,15 @@ def test_partition_with_more_replicas_than_slices(muon):
     assert owner == o_owner and load == o_load
     part = muon.Partition(plan, 8)
     assert part.owned(7) == [] and part.owned(0) != []
+
+
+def test_c_program_uses_the_abi(muon, tmp_path):
+    # plain C, linked against libmuon.so, host-only calls
+    import subprocess
+    src = os.path.join(ROOT, "tests", "c_abi_check.c")
+    exe = str(tmp_path / "c_abi_check")
+    libdir = os.path.dirname(muon.LIB_PATH)
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           src, "-o", exe, "-L", libdir, "-lmuon", "-Wl,-rpath," + libdir])
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
