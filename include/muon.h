@@ -229,8 +229,8 @@ MUON_API muon_status muon_step_static(const muon_plan_t* plan, void* const* para
                                       float lr, float beta, float wd, int nesterov,
                                       int ns_steps, const float* coeffs, void* stream);
 
-/* Kernel launches muon_step makes for this plan and ns_steps (for
- * accounting; no device call). */
+/* Kernel launches muon_step makes for this plan and ns_steps, for a step
+ * without O outputs (for accounting; no device call). */
 MUON_API muon_status muon_plan_launches(const muon_plan_t* plan, int ns_steps, int* out);
 
 /*

@@ -303,6 +303,15 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
                 off.inv, cnt, st.T == 0 ? 1 : 0);
   if (le != cudaSuccess) return le;
   size_t xin = off.X0, xout = off.X1;
+  // without O outputs the last product applies the parameter update itself,
+  // for slices stored in the working orientation (a transposed slice would
+  // take a read-modify-write per element in the GEMM epilogue, measured to
+  // stall the tensor pipe: those keep the separate epilogue kernel)
+  bool want_o = false;
+  for (int i = 0; i < ns; ++i) want_o = want_o || ptrs.O[i] != nullptr;
+  const bool fuse = sizeof(IT) == 2 && st.T > 0 && !want_o && !g.tr;
+  const float decay = 1.f - st.lr * st.wd;
+  const float lrs = st.lr * g.scale;
   if constexpr (sizeof(IT) == 2) {
     // fp16 operands: the three products on the tcgen05 tensor cores.  The
     // a and b terms of the step are folded into the operands, so that no
@@ -327,12 +336,19 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
       g2.diag = st.a;
       e = tc_gemm(g2, s);
       if (e != cudaSuccess) return e;
-      // X' = B' X, X as an N-major B operand; fp32 O on the last step
+      // X' = B' X, X as an N-major B operand; fp32 O on the last step, or
+      // there the update W' = W (1 - lr wd) - lr s O into the parameters
       TcGemm g3;
       g3.batch = ns; g3.stride = sws; g3.err = err_word; g3.skip = st.skip;
       g3.M = mp; g3.N = np; g3.K = mp;
       g3.A = ws + off.B; g3.B = ws + xin; g3.b_mn = 1;
       g3.D = ws + (last ? off.V : xout); g3.d_f32 = last ? 1 : 0;
+      if (last && fuse) {
+        g3.W = ptrs.W;
+        g3.w_f32 = g.dtype == MUON_F32 ? 1 : 0;
+        g3.wm = g.m; g3.wn = g.n; g3.wtr = g.tr;
+        g3.decay = decay; g3.lrs = lrs;
+      }
       e = tc_gemm(g3, s);
       if (e != cudaSuccess) return e;
       const size_t tmp = xin; xin = xout; xout = tmp;
@@ -371,8 +387,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   }
   const int tiles = (!g.tr && vec) ? (int)(((g.M + 31) / 32) * ((g.N + 127) / 128))
                                    : (int)(((g.M + 31) / 32) * ((g.N + 31) / 32));
-  const float decay = 1.f - st.lr * st.wd;
-  const float lrs = st.lr * g.scale;
+  if (fuse) return cudaSuccess;   // the last product updated the parameters
   if (g.dtype == MUON_BF16)
     return launch_k(epilogue_kernel<__nv_bfloat16>, dim3(tiles, ns), dim3(kNT), 0, s, true, ptrs,
                     g.M, g.N, np, (int)g.tr, vec, decay, lrs, st.skip, ws, sws, off.V);
@@ -382,7 +397,12 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
 
 }  // namespace
 
-int dense_launches(int ns_steps) { return 4 + 3 * ns_steps; }
+// front, finalize, normalize, 3 products per NS step, epilogue; in the
+// tensor-core mode the last product applies the update to slices that are
+// not transposed (no epilogue launch)
+int dense_launches(int ns_steps, int mode, int tr) {
+  return (mode == MUON_MODE_TC16 && ns_steps > 0 && !tr ? 3 : 4) + 3 * ns_steps;
+}
 
 namespace {
 // *found = 1 when any value of the chunk's gradients is inf or NaN

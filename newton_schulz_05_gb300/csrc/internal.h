@@ -84,7 +84,7 @@ cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& 
                                      int nslices, const StepArgs& st, char* ws,
                                      int* err_word, cudaStream_t s, bool pdl_first);
 
-int dense_launches(int ns_steps);
+int dense_launches(int ns_steps, int mode, int tr);   // per chunk, step without O outputs
 
 // Sets *found to 1 when any gradient value of the chunk is inf or NaN.
 cudaError_t launch_check_finite(const Group& g, const SlicePtrs& ptrs, int nslices, int* found,

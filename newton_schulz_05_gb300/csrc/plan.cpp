@@ -201,7 +201,7 @@ muon_status muon_plan_launches(const muon_plan_t* P, int ns_steps, int* out) {
     if (G.kernel == MUON_KERNEL_SKINNY) {
       n += (c + kMaxSlicesPerLaunch - 1) / kMaxSlicesPerLaunch;
     } else {
-      n += ((c + G.chunk - 1) / G.chunk) * dense_launches(ns_steps);
+      n += ((c + G.chunk - 1) / G.chunk) * dense_launches(ns_steps, P->opt.mode, G.tr);
     }
   }
   *out = n;

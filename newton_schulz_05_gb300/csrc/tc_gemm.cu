@@ -56,7 +56,49 @@ struct TcParams {
   uint32_t idesc128;   // M = 128, N = 128: tiles with one 128-column half to compute
   int* err;
   const int* skip;
+  // fused parameter update (last product of the step): the epilogue applies
+  // W' = W decay - lrs O to the parameter slices instead of storing O
+  int fuse;
+  int w_f32;           // parameter dtype fp32 (else bf16)
+  int wm, wn;          // working dims of a slice (m rows of O, n columns)
+  int wtr;             // the parameter is stored transposed ([n, m])
+  int wvec;            // rows of every slice start 16-byte aligned (not wtr)
+  float decay, lrs;
+  void* W[kMaxSlicesPerLaunch];
 };
+
+// W' = W decay - lrs O for the 32 outputs o[] of working row r, columns
+// [c0, c0 + 32) of slice W (stored [m, n], or [n, m] when transposed)
+template <typename PT>
+__device__ __forceinline__ void fused_update(const TcParams& p, PT* W, int r, int c0, const float* o) {
+  if (r >= p.wm) return;   // padding row
+  if (!p.wtr) {
+    PT* row = W + (size_t)r * p.wn + c0;
+    if (p.wvec && c0 + 32 <= p.wn) {
+      constexpr int E = 16 / sizeof(PT);   // elements per 16-byte access
+      #pragma unroll
+      for (int k = 0; k < 32 / E; ++k) {
+        uint4 u = reinterpret_cast<const uint4*>(row)[k];
+        PT* e = reinterpret_cast<PT*>(&u);
+        #pragma unroll
+        for (int i = 0; i < E; ++i) e[i] = from_f<PT>(fmaf(to_f(e[i]), p.decay, -p.lrs * o[k * E + i]));
+        reinterpret_cast<uint4*>(row)[k] = u;
+      }
+    } else {
+      #pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < p.wn) row[j] = from_f<PT>(fmaf(to_f(row[j]), p.decay, -p.lrs * o[j]));
+    }
+  } else {
+    // stored element (c, r): consecutive lanes (rows r) touch consecutive addresses
+    #pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (c0 + j < p.wn) {
+        PT* w = W + (size_t)(c0 + j) * p.wm + r;
+        *w = from_f<PT>(fmaf(to_f(*w), p.decay, -p.lrs * o[j]));
+      }
+  }
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -371,6 +413,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           v2[j] = fmaf(p.alpha2, v[j], d * p.diag2);
           v[j] = fmaf(p.alpha, v[j], d * p.diag);
         }
+        if (p.fuse) {
+          if (p.w_f32) fused_update<float>(p, static_cast<float*>(p.W[b]), row, col0, v);
+          else fused_update<__nv_bfloat16>(p, static_cast<__nv_bfloat16*>(p.W[b]), row, col0, v);
+          continue;
+        }
         // the staging buffer of this chunk is free once the stores issued from
         // it nbuf chunks ago have read it
         if (lane == 0) bulk_wait_read(nbuf - 1);
@@ -514,6 +561,20 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
   p.total_tiles = p.tiles_per_batch * g.batch;
   p.d_f32 = g.d_f32;
   p.has_d2 = g.D2 ? 1 : 0;
+  p.fuse = g.W ? 1 : 0;
+  if (g.W) {
+    if (g.batch > kMaxSlicesPerLaunch || g.sym || g.D2) return cudaErrorInvalidValue;
+    p.w_f32 = g.w_f32; p.wm = (int)g.wm; p.wn = (int)g.wn; p.wtr = g.wtr;
+    p.decay = g.decay; p.lrs = g.lrs;
+    int vec = g.wtr ? 0 : 1;
+    const size_t es = g.w_f32 ? 4 : 2;
+    if ((size_t)g.wn * es % 16) vec = 0;
+    for (int i = 0; i < g.batch; ++i) {
+      p.W[i] = g.W[i];
+      if (reinterpret_cast<uintptr_t>(g.W[i]) % 16) vec = 0;
+    }
+    p.wvec = vec;
+  }
   p.alpha = g.alpha; p.diag = g.diag;
   p.alpha2 = g.alpha2; p.diag2 = g.diag2;
   p.sym = g.sym; p.b_mn = g.b_mn;

@@ -32,6 +32,14 @@ struct TcGemm {
   float alpha2 = 1.f, diag2 = 0.f;
   int sym = 0;
   int b_mn = 0;
+  // fused parameter update (non-symmetric products only): with W set, the
+  // epilogue writes W'[b] = W[b] (1 - lr wd) - lrs D[b] into parameter slice
+  // b, of dtype bf16 (w_f32 = 0) or fp32, stored [wm, wn] or, with wtr, [wn, wm]
+  // (D's rows past wm and columns past wn are padding), and stores no D
+  void* const* W = nullptr;
+  int w_f32 = 0, wtr = 0;
+  int64_t wm = 0, wn = 0;
+  float decay = 1.f, lrs = 0.f;
   int* err = nullptr;   // device error word (bounded waits)
   const int* skip = nullptr;  // device flag: when set, the kernel returns at once
 };

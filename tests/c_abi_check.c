@@ -60,7 +60,10 @@ int main(void) {
   size_t ws = 0;
   CHECK(muon_plan_workspace_bytes(plan, &ws) == MUON_OK && ws > 256 && ws % 256 == 0);
   int launches = 0;
-  CHECK(muon_plan_launches(plan, 5, &launches) == MUON_OK && launches == 1 + 2 * 19);
+  /* one fused launch for the skinny group; per dense group front, finalize,
+   * normalize and three products per step, the last of which applies the
+   * update, plus an epilogue launch for the transposed group */
+  CHECK(muon_plan_launches(plan, 5, &launches) == MUON_OK && launches == 1 + 18 + 19);
 
   /* replicas: every slice has one owner, the loads sum up */
   int owner[78];
