@@ -232,13 +232,15 @@ struct SkinnySmem {
   static constexpr size_t ring = (misc + 64 * sizeof(float) + 16 + 127) & ~size_t(127);
   // ring of row stages (bulk copies), SW columns = one superchunk per warp;
   // row pitches padded so the fragment reads of a warp hit distinct banks.
-  // Pass 1 stages hold G and M rows, pass 2 stages only W rows, so the same
-  // bytes hold more pass-2 stages.
+  // Pass 1 stages hold G and M rows; pass 2 stages only W rows, two
+  // superchunks per warp (2 SW columns: half the copies and half the stage
+  // hand-offs of single-width stages).
   static constexpr int SW = 32 * NW;
   static constexpr int PITCH_G = SW * ES + (ES == 2 ? 32 : 64);
   static constexpr int PITCH_M = SW * 4 + 64;
   static constexpr size_t STAGE = (size_t)MP * (PITCH_G + PITCH_M);
-  static constexpr size_t STAGE_W = (size_t)MP * PITCH_G;
+  static constexpr int PITCH_W = 2 * SW * ES + (ES == 2 ? 32 : 64);
+  static constexpr size_t STAGE_W = (size_t)MP * PITCH_W;
   static constexpr size_t BUDGET = 224 * 1024 > ring ? 224 * 1024 - ring : 0;
   static constexpr int FIT = (int)(BUDGET / STAGE);
   static constexpr bool STAGED = !ALIAS && FIT >= 2;
@@ -434,7 +436,8 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   auto sc_col = [&](int q) { return (jc0 + warp + q * NW) * 32; };
 
   const int c_lo = jc0 * 32, c_hi = min(p.n, jc1 * 32);
-  const int nstage = jc1 > jc0 ? (c_hi - c_lo + S::SW - 1) / S::SW : 0;   // stages per pass
+  const int nstage = jc1 > jc0 ? (c_hi - c_lo + S::SW - 1) / S::SW : 0;   // pass-1 stages
+  const int nstage_w = (nstage + 1) / 2;                                      // pass-2 stages
   bool wait_ok = true;
   // Rows [part*R, (part+1)*R) of stage k of pass `w2` (0: G and M rows,
   // 1: W rows), columns [c_lo + k*SW, ...); one warp issues them, one row per
@@ -442,8 +445,9 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   // land first: the phase cannot complete before that arrive).
   auto issue_stage = [&](int k, int w2, int part = 0, int nparts = 1) {
     if (!S::STAGED) return;
-    const int c0 = c_lo + k * S::SW;
-    const int cols = min(S::SW, c_hi - c0);
+    const int width = w2 ? 2 * S::SW : S::SW;
+    const int c0 = c_lo + k * width;
+    const int cols = min(width, c_hi - c0);
     uint64_t* bar = w2 ? &full_w[k % NSTW] : &full[k % NSTG];
     unsigned char* base = smem + S::ring + (w2 ? (size_t)(k % NSTW) * S::STAGE_W : (size_t)(k % NSTG) * S::STAGE);
     if (part == 0 && lane == 0)
@@ -454,7 +458,8 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     const int r1 = min(p.m, (part + 1) * R);
     for (int i = part * R + lane; i < r1; i += 32) {
       const PT* src = w2 ? W : G;
-      bulk_load(base + i * S::PITCH_G, src + (size_t)i * p.n + c0, cols * (int)sizeof(PT), bar);
+      bulk_load(base + i * (w2 ? S::PITCH_W : S::PITCH_G), src + (size_t)i * p.n + c0,
+                cols * (int)sizeof(PT), bar);
       if (!w2)
         bulk_load(base + MP * S::PITCH_G + i * S::PITCH_M, Mo + (size_t)i * p.n + c0, cols * 4, bar);
     }
@@ -471,7 +476,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
       if (atomicAdd(cnt, 1) == NW - 1) { *cnt = 0; last = 1; }
     }
     last = __shfl_sync(0xffffffffu, last, 0);
-    if (last && k + depth < nstage) issue_stage(k + depth, w2);
+    if (last && k + depth < (w2 ? nstage_w : nstage)) issue_stage(k + depth, w2);
   };
   auto stage_wait = [&](int k, int w2) {
     uint64_t* bar = w2 ? &full_w[k % NSTW] : &full[k % NSTG];
@@ -642,7 +647,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   // warps issue the copies during it (issuing a bulk copy takes tens of
   // cycles, which would otherwise delay the reductions).
   if (staged && !SPLIT) {
-    const int ns0 = min(NSTW, nstage), parts = NW / NSTW;
+    const int ns0 = min(NSTW, nstage_w), parts = NW / NSTW;
     if (warp / parts < ns0) issue_stage(warp / parts, 1, warp % parts, parts);
   }
   __syncthreads();
@@ -701,9 +706,9 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     // one stage per idle warp, round robin; the last idle warp then warms L2
     // with the columns the ring does not hold yet
     constexpr int IW = (NT - RT) / 32;
-    const int ns0 = min(NSTW, nstage);
+    const int ns0 = min(NSTW, nstage_w);
     for (int k = warp - RT / 32; k < ns0; k += IW) issue_stage(k, 1);
-    if (warp == NW - 1) prefetch_w_l2(c_lo + ns0 * S::SW);
+    if (warp == NW - 1) prefetch_w_l2(c_lo + ns0 * 2 * S::SW);
     for (int t = 0; t < st.T; ++t) { float* x = mQ; mQ = mT1; mT1 = x; }
   }
   if constexpr (SPLIT) __syncthreads();
@@ -753,22 +758,24 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     const bool has = q < nslot;
     float wcur[MB][2][4];
     if (staged) {
-      stage_wait(q, 1);
-      const unsigned char* base = smem + S::ring + (size_t)(q % NSTW) * S::STAGE_W;
+      // superchunks q and q + 1 (q even) share one double-width stage
+      const int k2 = q >> 1;
+      if ((q & 1) == 0) stage_wait(k2, 1);
+      const unsigned char* base = smem + S::ring + (size_t)(k2 % NSTW) * S::STAGE_W;
       #pragma unroll
       for (int rb = 0; rb < MB; ++rb)
         #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int i = rb * 8 + g;
-          const int cl = warp * 32 + h * 16 + 4 * t4;
+          const int cl = (q & 1) * S::SW + warp * 32 + h * 16 + 4 * t4;
           const bool in = has && row_ok(rb) && sc_col(q) + h * 16 + 4 * t4 < p.n;
           if (in) {
             if constexpr (sizeof(PT) == 2) {
-              const uint2 u = *reinterpret_cast<const uint2*>(base + i * S::PITCH_G + cl * 2);
+              const uint2 u = *reinterpret_cast<const uint2*>(base + i * S::PITCH_W + cl * 2);
               const float2 x = unpack_bf16(u.x), y = unpack_bf16(u.y);
               wcur[rb][h][0] = x.x; wcur[rb][h][1] = x.y; wcur[rb][h][2] = y.x; wcur[rb][h][3] = y.y;
             } else {
-              const float4 u = *reinterpret_cast<const float4*>(base + i * S::PITCH_G + cl * 4);
+              const float4 u = *reinterpret_cast<const float4*>(base + i * S::PITCH_W + cl * 4);
               wcur[rb][h][0] = u.x; wcur[rb][h][1] = u.y; wcur[rb][h][2] = u.z; wcur[rb][h][3] = u.w;
             }
           } else {
@@ -776,7 +783,8 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
             for (int e = 0; e < 4; ++e) wcur[rb][h][e] = 0.f;
           }
         }
-      release_stage(q, 1);
+      // the stage is handed back after its second superchunk (or the last)
+      if ((q & 1) == 1 || q + 1 == npass) release_stage(k2, 1);
     } else {
       #pragma unroll
       for (int rb = 0; rb < MB; ++rb)
