@@ -31,9 +31,12 @@
 //   * ||V||^2 and V V^T are reduced deterministically: warps -> CTA in shared
 //     memory, CTAs -> cluster through distributed shared memory in rank
 //     order, so every CTA holds the same bits and computes the same Q in fp32;
-//   * gradient and momentum rows are prefetched into L2 a few superchunks
-//     ahead, the parameter rows while Q is being formed, and the parameter
-//     loads of the update are issued one superchunk ahead.
+//   * rows stream through a shared-memory ring of bulk copies when they are
+//     16-byte aligned (G and M rows in pass 1, W rows in pass 2, the first W
+//     stages issued by the warps the m x m recursion leaves idle); otherwise
+//     gradient and momentum rows are prefetched into L2 a few superchunks
+//     ahead and the parameter loads of the update are issued one superchunk
+//     ahead.
 #include <cooperative_groups.h>
 #include <cstdio>
 
@@ -440,8 +443,8 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   const int nstage_w = (nstage + 1) / 2;                                      // pass-2 stages
   bool wait_ok = true;
   // Rows [part*R, (part+1)*R) of stage k of pass `w2` (0: G and M rows,
-  // 1: W rows), columns [c_lo + k*SW, ...); one warp issues them, one row per
-  // lane.  Part 0 posts the stage's byte count (copies of other parts may
+  // columns [c_lo + k*SW, ...); 1: W rows, columns [c_lo + 2k*SW, ...)); one
+  // warp issues them, one row per lane.  Part 0 posts the stage's byte count (copies of other parts may
   // land first: the phase cannot complete before that arrive).
   auto issue_stage = [&](int k, int w2, int part = 0, int nparts = 1) {
     if (!S::STAGED) return;
@@ -737,7 +740,6 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     }
 
   // ---- pass 2: O = Q X_0 and W' = W (1 - lr wd) - lr s O -------------------------
-  // (the ring held the m x m matrices until the barrier above)
   float wbuf[MB][2][4];
   auto load_w = [&](int q) {
     const int cb = sc_col(q);
