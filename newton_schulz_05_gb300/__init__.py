@@ -498,3 +498,53 @@ class ShardedMuon:
         self.update_owned(grads, stream)
         if self.world > 1:
             self.partition.broadcast(self.params, self.group)
+
+
+class MuonWithAdamW:
+    """Muon for the matrix parameters (2-D matrices and 3-D [E, M, N] stacks)
+    and AdamW for the others (1-D biases and norm scales): the split of the
+    Paddle Muon sharding PR ("Support Muon sharding optimizer comm overlap"),
+    which keeps 2-D and 1-D gradients in separate buffers because the two
+    kinds of parameter take different update rules.
+
+    ``step(grads)`` takes the gradients in the order of ``params`` and runs
+    one muon_step over the matrix parameters and one muon_adamw_step per
+    dtype over the others, all on the stream."""
+
+    def __init__(self, params: Sequence[torch.Tensor], lr: float = 0.02, beta: float = 0.95,
+                 wd: float = 0.1, nesterov: bool = True, ns_steps: int = 5,
+                 coeffs=DEFAULT_COEFFS, mode: str = "tc16", eps: float = 1e-7,
+                 adamw_lr: float = 3e-4, betas=(0.9, 0.999), adamw_eps: float = 1e-8,
+                 adamw_wd: float = 0.0):
+        self.params = list(params)
+        self.matrix_idx, self.other_idx, self.groups = self.route(self.params)
+        mats = [self.params[i] for i in self.matrix_idx]
+        self.muon = Muon(mats, lr=lr, beta=beta, wd=wd, nesterov=nesterov, ns_steps=ns_steps,
+                         coeffs=coeffs, mode=mode, eps=eps) if mats else None
+        self.exp_avg = {i: torch.zeros(self.params[i].numel(), dtype=torch.float32,
+                                       device=self.params[i].device) for i in self.other_idx}
+        self.exp_avg_sq = {i: torch.zeros_like(self.exp_avg[i]) for i in self.other_idx}
+        self.adamw = dict(lr=adamw_lr, beta1=betas[0], beta2=betas[1], eps=adamw_eps, wd=adamw_wd)
+        self.t = 0
+
+    @staticmethod
+    def route(params: Sequence[torch.Tensor]):
+        """(indices of the Muon parameters, indices of the AdamW parameters,
+        {dtype: AdamW indices}) for a parameter list."""
+        matrix = [i for i, p in enumerate(params) if p.dim() in (2, 3)]
+        other = [i for i, p in enumerate(params) if p.dim() not in (2, 3)]
+        groups = {}
+        for i in other:
+            groups.setdefault(params[i].dtype, []).append(i)
+        return matrix, other, groups
+
+    def step(self, grads: Sequence[torch.Tensor], stream=None) -> None:
+        if len(grads) != len(self.params):
+            raise ValueError("expected one gradient per parameter")
+        self.t += 1
+        if self.muon is not None:
+            self.muon.step([grads[i] for i in self.matrix_idx], stream=stream)
+        for _, idx in self.groups.items():
+            adamw_step([self.params[i].view(-1) for i in idx], [grads[i].reshape(-1) for i in idx],
+                       [self.exp_avg[i] for i in idx], [self.exp_avg_sq[i] for i in idx],
+                       step=self.t, stream=stream, **self.adamw)

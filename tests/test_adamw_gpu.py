@@ -88,3 +88,26 @@ def test_adamw_zero_lr_keeps_params():
                  [torch.zeros(w.numel(), device="cuda") for w in W], lr=0.0, wd=0.1, step=1)
     torch.cuda.synchronize()
     assert all(torch.equal(a, b) for a, b in zip(W, W0))
+
+
+def test_muon_with_adamw_equals_the_separate_steps():
+    # one MuonWithAdamW step == Muon on the matrices + AdamW on the rest, bit for bit
+    m = muon()
+    shapes = [(24, 1000), (300,), (2, 200, 150), (77,), (5,)]
+    dts = [torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.float32, torch.bfloat16]
+    P = [synth.draw(s, 0.02, synth.param_seed(1, i), d, "cuda") for i, (s, d) in enumerate(zip(shapes, dts))]
+    G = [synth.draw(s, 1e-2, synth.param_seed(2, i), d, "cuda") for i, (s, d) in enumerate(zip(shapes, dts))]
+    P2 = [p.clone() for p in P]
+    opt = m.MuonWithAdamW(P, adamw_lr=1e-3, adamw_wd=0.01)
+    for _ in range(2):
+        opt.step(G)
+    ref_muon = m.Muon([P2[0], P2[2]])
+    mom = {i: (torch.zeros(P2[i].numel(), device="cuda"), torch.zeros(P2[i].numel(), device="cuda"))
+           for i in (1, 3, 4)}
+    for t in (1, 2):
+        ref_muon.step([G[0], G[2]])
+        for idx in ([1, 4], [3]):
+            m.adamw_step([P2[i].view(-1) for i in idx], [G[i].reshape(-1) for i in idx],
+                         [mom[i][0] for i in idx], [mom[i][1] for i in idx], lr=1e-3, wd=0.01, step=t)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(P, P2))

@@ -267,3 +267,16 @@ def test_c_program_uses_the_abi(muon, tmp_path):
                            src, "-o", exe, "-L", libdir, "-lmuon", "-Wl,-rpath," + libdir])
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def test_muon_with_adamw_routes_parameters(muon):
+    # matrices and stacks to Muon, the rest to AdamW grouped by dtype
+    import torch
+    params = [torch.zeros(24, 64, dtype=torch.bfloat16), torch.zeros(64, dtype=torch.bfloat16),
+              torch.zeros(2, 24, 64, dtype=torch.bfloat16), torch.zeros(10),
+              torch.zeros(3, dtype=torch.bfloat16)]
+    matrix, other, groups = muon.MuonWithAdamW.route(params)
+    assert matrix == [0, 2] and other == [1, 3, 4]
+    assert groups == {torch.bfloat16: [1, 4], torch.float32: [3]}
+    plan = muon.Plan([params[i] for i in matrix])
+    assert plan.num_slices == 3
