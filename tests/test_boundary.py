@@ -280,3 +280,26 @@ def test_muon_with_adamw_routes_parameters(muon):
     assert groups == {torch.bfloat16: [1, 4], torch.float32: [3]}
     plan = muon.Plan([params[i] for i in matrix])
     assert plan.num_slices == 3
+
+
+def test_skinny_plans_fit_the_cluster_tensor_memory(muon):
+    # V is held in bf16 in tensor memory between the passes: the slice (rows
+    # padded to a block of 8, columns to 32) must fit the cluster's CTAs,
+    # each with 128 lanes x 512 columns x 4 bytes; clusters are portable (<= 8)
+    import torch
+    tmem_cta = 128 * 512 * 4
+    for m_ in list(range(1, 65, 3)) + [64]:
+        for n_ in (m_, 77, 1000, 10240, 40000, 65536, 100000, 200000):
+            if n_ < m_:
+                continue
+            plan = muon.Plan([((m_, n_), torch.bfloat16)])
+            (g,) = plan.groups()
+            if g["kernel"] != muon.KERNEL_SKINNY:
+                continue
+            mp8 = (m_ + 7) // 8 * 8
+            n32 = (n_ + 31) // 32 * 32
+            assert 1 <= g["cluster"] <= 8, (m_, n_)
+            assert mp8 * n32 * 2 <= g["cluster"] * tmem_cta, (m_, n_, g["cluster"])
+    # a slice too long for 8 CTAs goes to the dense path
+    (g,) = muon.Plan([((64, 1 << 20), torch.bfloat16)]).groups()
+    assert g["kernel"] == muon.KERNEL_DENSE
