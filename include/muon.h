@@ -217,17 +217,31 @@ MUON_API muon_status muon_workspace_error(const void* workspace, void* stream, i
  * that size are rejected with MUON_ERR_WORKSPACE before any device work.
  * The first call on each device, with that device current, looks up the
  * array's device address and caches it; make that first call before any
- * stream capture.  Every call shares the array and finds the previous call's
- * contents there: the device error word is cleared at each call, everything
- * else is written before it is read.  Calls whose work overlaps on the GPU
- * (streams with no ordering between them) race on the array.  Arguments are
- * those of muon_step.
+ * stream capture.  The cache assumes the device is not reset
+ * (cudaDeviceReset) while the library is loaded.  `stream` must belong to the
+ * current device (else MUON_ERR_INVALID_ARG).  Every call shares the array
+ * and finds the previous call's contents there: the device error word is
+ * cleared at each call, everything else is written before it is read.  Calls
+ * whose work overlaps on the GPU (streams with no ordering between them) race
+ * on the array.  A device-side wait that gave up during the step is reported
+ * by muon_static_error, not by the return code.  Other arguments are those of
+ * muon_step.
  */
 #define MUON_STATIC_WORKSPACE_BYTES (32u << 20)
 MUON_API muon_status muon_step_static(const muon_plan_t* plan, void* const* params,
                                       const void* const* grads, float* const* momentum,
                                       float lr, float beta, float wd, int nesterov,
                                       int ns_steps, const float* coeffs, void* stream);
+
+/*
+ * The device error word that the last muon_step_static on the current device
+ * left in the static array, read after synchronising `stream` (which must
+ * belong to the current device): *code receives MUON_OK or
+ * MUON_ERR_DEVICE_TIMEOUT; when clear != 0 the word is reset to zero.  Call
+ * it before the next muon_step_static, which clears the word.  Allocates
+ * nothing.  The RFC has no counterpart of this call.
+ */
+MUON_API muon_status muon_static_error(void* stream, int clear, int* code);
 
 /* Kernel launches muon_step makes for this plan and ns_steps, for a step
  * without O outputs (for accounting; no device call). */

@@ -58,7 +58,7 @@ EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
            "muon_plan_num_groups", "muon_plan_num_slices", "muon_plan_group",
            "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
            "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static",
-           "muon_step_amp", "muon_adamw_step", "muon_plan_partition"]
+           "muon_step_amp", "muon_adamw_step", "muon_plan_partition", "muon_static_error"]
 
 STATIC_WORKSPACE_BYTES = 32 << 20   # MUON_STATIC_WORKSPACE_BYTES in include/muon.h
 
@@ -101,6 +101,7 @@ def load(path: str = LIB_PATH):
                                   ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                   ctypes.c_float, ctypes.c_float, ctypes.c_int, vp]
     L.muon_workspace_error.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    L.muon_static_error.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.muon_plan_launches.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.muon_plan_partition.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                       ctypes.c_double, ctypes.POINTER(ctypes.c_int),
@@ -112,7 +113,8 @@ def load(path: str = LIB_PATH):
     for fn in ("muon_plan", "muon_plan_workspace_bytes", "muon_plan_num_groups",
                "muon_plan_num_slices", "muon_plan_group", "muon_plan_slice", "muon_step",
                "muon_step_ortho", "muon_workspace_error", "muon_plan_launches",
-               "muon_step_static", "muon_step_amp", "muon_adamw_step", "muon_plan_partition"):
+               "muon_step_static", "muon_step_amp", "muon_adamw_step", "muon_plan_partition",
+               "muon_static_error"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -275,6 +277,16 @@ def step_static(plan: Plan, params, grads, momentum, *, lr: float, beta: float, 
     _check(load().muon_step_static(plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum), lr,
                                    beta, wd, int(bool(nesterov)), ns_steps, c,
                                    ctypes.c_void_p(_stream_handle(stream))), "muon_step_static")
+
+
+def static_error(stream=None, clear: bool = True) -> int:
+    """Device error word that the last step_static on the current device left
+    in the library's static scratch (synchronises the stream); 0 when every
+    device-side wait of that step completed."""
+    code = ctypes.c_int()
+    _check(load().muon_static_error(ctypes.c_void_p(_stream_handle(stream)), int(clear),
+                                    ctypes.byref(code)), "static_error")
+    return code.value
 
 
 def step_amp(plan: Plan, params, grads, momentum, *, lr: float, beta: float, wd: float,
