@@ -53,6 +53,18 @@ void parallel_rows(int64_t rows, int threads, F fn) {
   for (auto& th : pool) th.join();
 }
 
+// Run fn(i) for every row i of [0, rows), rows dealt to `threads` workers
+// in turn (row i to worker i mod threads), for rows of unequal cost.
+template <class F>
+void parallel_rows_dealt(int64_t rows, int threads, F fn) {
+  int t = (int)std::max<int64_t>(1, std::min<int64_t>(threads, rows));
+  if (t == 1) { for (int64_t i = 0; i < rows; ++i) fn(i); return; }
+  std::vector<std::thread> pool;
+  for (int w = 0; w < t; ++w)
+    pool.emplace_back([=] { for (int64_t i = w; i < rows; i += t) fn(i); });
+  for (auto& th : pool) th.join();
+}
+
 }  // namespace
 
 extern "C" {
@@ -131,7 +143,10 @@ void oracle_normalize(int64_t count, const double* V, double eps, double* X_out)
 // transposed back, so O always has X's shape.  Each step:
 //   A = X X^T;  B = b*A + c*(A A);  X <- a*X + B X.
 // `threads` splits the rows of each product across workers; every output
-// entry is still one plain sum in index order.
+// entry is still one plain sum in index order.  X X^T and A A are symmetric
+// by definition: entry (j, i) of either is the sum of the same products as
+// entry (i, j), in the same order (A itself is exactly symmetric), so it is
+// the same number; each is computed for j >= i and copied to (j, i).
 void oracle_newton_schulz(int64_t M, int64_t N, const double* X_in, int T,
                           double a, double b, double c, int threads,
                           double* O_out) {
@@ -143,27 +158,29 @@ void oracle_newton_schulz(int64_t M, int64_t N, const double* X_in, int T,
       X[i * n + k] = tr ? X_in[k * N + i] : X_in[i * n + k];
   std::vector<double> A((size_t)(m * m)), At((size_t)(m * m)), B((size_t)(m * m));
   for (int t = 0; t < T; ++t) {
-    // A = X X^T
-    parallel_rows(m, threads, [&](int64_t r0, int64_t r1) {
-      for (int64_t i = r0; i < r1; ++i)
-        for (int64_t j = 0; j < m; ++j) {
-          double acc = 0.0;
-          for (int64_t k = 0; k < n; ++k) acc += X[i * n + k] * X[j * n + k];
-          A[i * m + j] = acc;
-        }
+    // A = X X^T (upper triangle, then mirrored)
+    parallel_rows_dealt(m, threads, [&](int64_t i) {
+      for (int64_t j = i; j < m; ++j) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < n; ++k) acc += X[i * n + k] * X[j * n + k];
+        A[i * m + j] = acc;
+      }
     });
+    for (int64_t i = 0; i < m; ++i)
+      for (int64_t j = 0; j < i; ++j) A[i * m + j] = A[j * m + i];
     // B = b*A + c*(A A); the second factor is read from a transposed copy
     // At[j][k] = A[k][j] so that both operands stream along rows
     for (int64_t i = 0; i < m; ++i)
       for (int64_t j = 0; j < m; ++j) At[j * m + i] = A[i * m + j];
-    parallel_rows(m, threads, [&](int64_t r0, int64_t r1) {
-      for (int64_t i = r0; i < r1; ++i)
-        for (int64_t j = 0; j < m; ++j) {
-          double acc = 0.0;
-          for (int64_t k = 0; k < m; ++k) acc += A[i * m + k] * At[j * m + k];
-          B[i * m + j] = b * A[i * m + j] + c * acc;
-        }
+    parallel_rows_dealt(m, threads, [&](int64_t i) {
+      for (int64_t j = i; j < m; ++j) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < m; ++k) acc += A[i * m + k] * At[j * m + k];
+        B[i * m + j] = b * A[i * m + j] + c * acc;
+      }
     });
+    for (int64_t i = 0; i < m; ++i)
+      for (int64_t j = 0; j < i; ++j) B[i * m + j] = B[j * m + i];
     // X <- a*X + B X
     parallel_rows(m, threads, [&](int64_t r0, int64_t r1) {
       std::vector<double> row((size_t)n);
