@@ -5,16 +5,21 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 A step is one muon_step over every parameter of the workload (momentum,
 normalisation, 5 Newton-Schulz steps, weight-decay update).  The default
-workload is 74 separate bf16 [24, 10240] parameters grouped into one
-[74, 24, 10240] batch (the small-parameter case of the HyperParallel FSDP
-Muon RFC, section 3).  Inputs are seeded synthetic tensors generated on the
-device.  L2 is flushed (512 MB write) before every timed step; each step is
-timed with CUDA events on the launching stream and ms_per_step is their
-mean, max over ranks.
+workload is the largest single-GPU one: the parameter matrices of 24 dense
+transformer layers, 4 x [4096, 4096], [11008, 4096] and 2 x [4096, 11008]
+bf16 per layer (168 slices in three groups, 4.86 G parameters).  Other
+workloads (--workload): 74 separate bf16 [24, 10240] parameters grouped into
+one [74, 24, 10240] batch (the small-parameter case of the HyperParallel FSDP
+Muon RFC, section 3), 3-D stacks plus expert tensors, a synthetic MoE model.
+Inputs are seeded synthetic tensors generated on the device.  L2 is flushed
+(512 MB write) before every timed step; each step is timed with CUDA events
+on the launching stream and ms_per_step is their mean, max over ranks.
 
 --impl reference times the fp64 CPU oracle on the host cores on the same
-workload (a bounded sample of slices per step) and prints the same line
-with "impl": "reference".  Under torchrun only rank 0 runs it.
+workload (per step a bounded sample of every group, extrapolated to the
+whole workload by the Newton-Schulz flop count where a whole slice does not
+fit the step's time budget) and prints the same line with
+"impl": "reference".  Under torchrun only rank 0 runs it.
 
 With N > 1 (torchrun) each rank runs its own replica of the workload on its
 own GPU: slices are independent, there is no data-path collective
@@ -183,52 +188,111 @@ def skinny_traffic(per_launch_units):
 
 
 # ---------------------------------------------------------------- oracle leg
-def oracle_rate(w, budget_s: float, threads: int):
-    """Time the fp64 oracle on slices of the workload for about budget_s
-    seconds.  Returns (matrices/s for the whole workload, sample text)."""
-    import oracle
+def _ns_flops(m, n, T):
+    return T * (4 * m * m * n + 2 * m ** 3)
 
-    oracle.build()
-    shapes = list(w.shapes)
-    per_group = {}
-    for i, s in enumerate(shapes):
-        E, M, N = (s if len(s) == 3 else (1,) + tuple(s))
-        per_group.setdefault((M, N), [0, i])[0] += E
-    total_slices = sum(c for c, _ in per_group.values())
-    t_total = 0.0
-    notes = []
-    t_start = time.time()
-    for (M, N), (count, pidx) in per_group.items():
-        m, n = min(M, N), max(M, N)
-        fl = w.ns_steps * (4 * m * m * n + 2 * m ** 3)
-        # slices timed for this group: as many as fit the budget share, at least 1
-        W = synth.draw((M, N), w.param_std, synth.param_seed(1, pidx), w.dtype)
-        G = synth.draw((M, N), w.grad_std, synth.param_seed(0, pidx), w.dtype)
-        Mo = torch.zeros((M, N), dtype=torch.float32)
-        if fl > 50e9:
-            # a single slice would exceed the budget: time T=1 and scale by flops
-            t0 = time.time()
-            oracle.muon_slice(W, G, Mo, w.lr, w.beta, w.wd, w.nesterov, T=1, coeffs=w.coeffs,
-                              threads=threads)
-            dt = time.time() - t0
-            fl1 = 4 * m * m * n + 2 * m ** 3
-            t_slice = dt * fl / fl1
-            notes.append("%dx%d: 1 slice, 1 NS step, scaled by flops" % (M, N))
+
+class OracleSampler:
+    """The fp64 oracle timed on a bounded sample of a workload, extrapolated
+    to the whole workload.
+
+    Per bucket of equal (M, N) one slice is drawn with the workload's seeded
+    recipe.  When the oracle's whole step on that slice fits the bucket's
+    share of the time budget, whole slices are timed (as many as the host
+    threads run side by side); otherwise the oracle's whole step runs on the
+    first r working rows of the slice (columns when M > N), r chosen to fit
+    the budget, and its time is scaled to the full slice by the standard
+    Newton-Schulz flop count T (4 m^2 n + 2 m^3), which dominates the step
+    for such slices.  Bucket times are scaled by the bucket's slice count."""
+
+    def __init__(self, w, threads: int):
+        import oracle
+
+        oracle.build()
+        self.oracle = oracle
+        self.w = w
+        self.threads = threads
+        self.buckets = {}
+        for i, s in enumerate(w.shapes):
+            E, M, N = (s if len(s) == 3 else (1,) + tuple(s))
+            self.buckets.setdefault((M, N), [0, i])[0] += E
+        self.total_slices = sum(c for c, _ in self.buckets.values())
+        self.inputs = {}
+        for (M, N), (_, pidx) in self.buckets.items():
+            W = synth.draw((M, N), w.param_std, synth.param_seed(1, pidx), w.dtype)
+            G = synth.draw((M, N), w.grad_std, synth.param_seed(0, pidx), w.dtype)
+            self.inputs[(M, N)] = (W, G, torch.zeros((M, N), dtype=torch.float32))
+        self.rate = None   # oracle flops/s, from the first sample
+
+    def _run(self, W, G, Mo, k):
+        """k copies of one slice: side by side on the host threads, or one
+        slice with its products' rows spread over them."""
+        w = self.w
+        if k == 1:
+            self.oracle.muon_slice(W, G, Mo, w.lr, w.beta, w.wd, w.nesterov, T=w.ns_steps,
+                                   coeffs=w.coeffs, threads=self.threads)
+            return
+        self.oracle.muon_slices([W] * k, [G] * k, [Mo] * k, w.lr, w.beta, w.wd, w.nesterov,
+                                T=w.ns_steps, coeffs=w.coeffs, threads=self.threads,
+                                want_O=False)
+
+    def sample(self, budget_s: float):
+        """Time one sample of every bucket; returns (extrapolated seconds for
+        one step of the whole workload, sample description)."""
+        T = self.w.ns_steps
+        share = budget_s / len(self.buckets)
+        total, notes = 0.0, []
+        for (M, N), (count, _) in self.buckets.items():
+            W, G, Mo = self.inputs[(M, N)]
+            m, n = min(M, N), max(M, N)
+            full = max(_ns_flops(m, n, T), 1)
+            if self.rate is None:
+                # calibration: a small sub-block (or the whole slice if small)
+                r = min(m, 64)
+                t0 = time.perf_counter()
+                self._sub(W, G, Mo, M, N, r)
+                dt = time.perf_counter() - t0
+                self.rate = max(_ns_flops(r, n, T), 1) / max(dt, 1e-6)
+            if full / self.rate <= share:
+                k = max(1, min(count, self.threads))
+                t0 = time.perf_counter()
+                self._run(W, G, Mo, k)
+                dt = time.perf_counter() - t0
+                total += dt / k * count
+                notes.append("[%d,%d]: %d whole slice%s" % (M, N, k, "s" if k > 1 else ""))
+                self.rate = k * full / max(dt, 1e-9)
+            else:
+                r = int((share * self.rate / (T * (4 * n + 2 * m) + 1e-9)) ** 0.5)
+                r = max(8, min(m, r // 8 * 8))
+                # solve 4 r^2 n + 2 r^3 ~ share * rate more exactly
+                while r > 8 and _ns_flops(r, n, T) > share * self.rate:
+                    r -= 8
+                t0 = time.perf_counter()
+                self._sub(W, G, Mo, M, N, r)
+                dt = time.perf_counter() - t0
+                sub = max(_ns_flops(r, n, T), 1)
+                total += dt * full / sub * count
+                notes.append("[%d,%d]: first %d of %d working rows, scaled by flops" % (M, N, r, m))
+                self.rate = sub / max(dt, 1e-9)
+        return total, "; ".join(notes)
+
+    def _sub(self, W, G, Mo, M, N, r):
+        if M <= N:
+            self._run(W[:r].contiguous(), G[:r].contiguous(), Mo[:r].contiguous(), 1)
         else:
-            k = max(1, min(count, threads))
-            t0 = time.time()
-            reps = 0
-            while True:
-                oracle.muon_slices([W] * k, [G] * k, [Mo] * k, w.lr, w.beta, w.wd, w.nesterov,
-                                   T=w.ns_steps, coeffs=w.coeffs, threads=threads, want_O=False)
-                reps += 1
-                if time.time() - t0 > budget_s / len(per_group):
-                    break
-            t_slice = (time.time() - t0) / (reps * k)
-            notes.append("%dx%d: %d slices" % (M, N, reps * k))
-        t_total += t_slice * count
-    rate = total_slices / t_total
-    return rate, "; ".join(notes), time.time() - t_start
+            self._run(W[:, :r].contiguous(), G[:, :r].contiguous(), Mo[:, :r].contiguous(), 1)
+
+
+def oracle_rate(w, budget_s: float, threads: int):
+    """The oracle's throughput on the workload (matrices/s), from about
+    budget_s seconds of samples.  Returns (rate, sample text, seconds used)."""
+    t_start = time.time()
+    smp = OracleSampler(w, threads)
+    smp.sample(min(2.0, budget_s / 4))        # warm-up and rate calibration
+    t_step, notes = smp.sample(budget_s)
+    rate = smp.total_slices / t_step
+    extra = "" if "whole" in notes and "scaled" not in notes else "; extrapolated"
+    return rate, notes + extra, time.time() - t_start
 
 
 def run_reference(args, w):
@@ -236,50 +300,27 @@ def run_reference(args, w):
     if rank != 0:
         return
     threads = os.cpu_count() or 1
-    import oracle
-
-    oracle.build()
-    # each step: the oracle over a bounded sample of the workload's slices
-    slices = []
-    for i, s in enumerate(w.shapes):
-        E, M, N = (s if len(s) == 3 else (1,) + tuple(s))
-        for e in range(E):
-            slices.append((i, M, N))
-    budget_per_step = max(0.05, 150.0 / max(1, args.steps + args.warmup))
-    # probe one slice to size the sample
-    i, M, N = slices[0]
-    W = synth.draw((M, N), w.param_std, synth.param_seed(1, i), w.dtype)
-    G = synth.draw((M, N), w.grad_std, synth.param_seed(0, i), w.dtype)
-    Mo = torch.zeros((M, N), dtype=torch.float32)
-    big = max(min(Mx, Nx) ** 2 * max(Mx, Nx) for _, Mx, Nx in slices) > 2e10
-    if big:
-        print(json.dumps({"impl": "reference", "unavailable":
-                          "the fp64 oracle needs minutes per slice of this workload; "
-                          "the reference arm runs on the skinny workloads only"}))
-        return
-    t0 = time.time()
-    oracle.muon_slices([W] * threads, [G] * threads, [Mo] * threads, w.lr, w.beta, w.wd,
-                       w.nesterov, T=w.ns_steps, coeffs=w.coeffs, threads=threads, want_O=False)
-    per_round = time.time() - t0
-    rounds = max(1, int(budget_per_step / per_round))
-    k = min(len(slices), rounds * threads)
-    Ws = [W] * k; Gs = [G] * k; Ms = [Mo] * k
+    smp = OracleSampler(w, threads)
+    # every step: one bounded sample of the workload, sized so that the whole
+    # --steps K --warmup W run takes about 150 s of host time
+    budget_per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    smp.sample(min(2.0, budget_per_step))   # rate calibration
     times = []
+    notes = ""
     for it in range(args.warmup + args.steps):
-        t0 = time.time()
-        oracle.muon_slices(Ws, Gs, Ms, w.lr, w.beta, w.wd, w.nesterov, T=w.ns_steps,
-                           coeffs=w.coeffs, threads=threads, want_O=False)
+        t_step, notes = smp.sample(budget_per_step)
         if it >= args.warmup:
-            times.append(time.time() - t0)
+            times.append(t_step)
     t = sum(times) / len(times)
-    rate = k / t
-    ms_step = 1e3 * len(slices) / rate
-    sample = "%d of %d slices per step (%dx%d), fp64 oracle, %d threads" % (
-        k, len(slices), M, N, threads)
+    rate = smp.total_slices / t
+    extrapolated = "scaled" in notes or any(
+        c > min(c, threads) for c, _ in smp.buckets.values())
+    sample = "per step, fp64 oracle on %d threads: %s%s" % (
+        threads, notes, "; extrapolated to all %d slices" % smp.total_slices if extrapolated else "")
     out = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "config": {"workload": w.name, "slices": len(slices)},
+           "data": "synthetic", "config": {"workload": w.name, "slices": smp.total_slices},
            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                             "sample": sample},
            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -460,10 +501,10 @@ def run_ours(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="skinny_74x24x10240", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="dense_24L", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ns-steps", type=int, default=None,
                     help="Newton-Schulz steps T (default: the workload's, 5); T = 0 times "

@@ -106,6 +106,10 @@ WORKLOADS = {
     # synthetic MoE model, about 3.7 B parameters
     "moe_24L": Workload(
         "moe_24L", _moe_layers(24), torch.bfloat16, grad_std=1e-2),
+    # one layer of the dense set: the 4096-class products at a size for
+    # kernel profiles (about 4 GB on the device with its workspace)
+    "dense_1L": Workload(
+        "dense_1L", _dense_layers(1), torch.bfloat16, grad_std=1e-3),
     # one expert stack of the MoE model: the small dense case used for
     # kernel profiles (about 1.2 GB on the device with its workspace)
     "experts_16x1408x2048": Workload(

@@ -158,3 +158,55 @@ def run_and_check(shapes, dtype, hp, mode="tc16", grad_std=1e-2, seed=0, which=N
         compare((p, e), gp, r, slices(W[p])[e], slices(G[p])[e], slices(M[p])[e], hp, mode, dtype,
                 report)
     return plan
+
+
+def compare_folded(key, Wf, W0, G, M0, Og, ref, hp, dtype):
+    """Assert one slice's parameters from the step WITHOUT an O output
+    against the oracle, element by element.
+
+    On the fused skinny kernel that step folds the update factor -lr*s into
+    the 16-bit left operand of its last product: it computes
+    sum_k RNE16(-lr*s*Q~_ik) V_kj instead of -lr*s * sum_k RNE16(Q~_ik) V_kj,
+    with Q~ = Q/(||V|| + eps) and O = Q X0.  The two left operands differ by
+    at most 2^-8 relative per entry (one extra rounding of each, 2^-9 apiece;
+    bf16 has 8 significant bits), so the update term differs from the one of
+    the step that writes O (Og, same kernel, same V and fp32 Q bits) by at
+    most lr*s*2^-8*(|Q| |X0|)_ij.  Q is recovered from the oracle in fp64 as
+    the m x m matrix with O = Q X0 (X0 has full row rank).  The bound per
+    parameter, against the round-to-nearest value of the oracle's W':
+      ulp + lr*s*|Og - O_oracle| + 1.05 * lr*s*2^-8*(|Q| |X0|) + 4*2^-24*terms
+    (the 5% covers the fp32 Q of the kernel against the fp64 one).  On the
+    dense path the step without O is the same arithmetic as the one with O,
+    so there the last two terms of the bound are not needed (the tests check
+    those parameters bit for bit against the O-writing step as well)."""
+    Wf = np.asarray(Wf.double().cpu().numpy(), np.float64)
+    W0 = np.asarray(W0.double().cpu().numpy(), np.float64)
+    G = np.asarray(G.double().cpu().numpy(), np.float64)
+    M0 = np.asarray(M0.double().cpu().numpy(), np.float64)
+    Og = np.asarray(Og.double().cpu().numpy(), np.float64)
+    Wr, _, Or = ref
+    M_, N_ = W0.shape
+    s = float(np.float32(np.sqrt(max(1.0, M_ / N_))))
+    lrs = hp["lr"] * s
+    Mp = hp["beta"] * M0 + G
+    V = G + hp["beta"] * Mp if hp["nesterov"] else Mp
+    X0 = V / (np.linalg.norm(V) + 1e-7)
+    Xw, Ow = (X0.T, Or.T) if M_ > N_ else (X0, Or)
+    # O = Q X0  ->  Q = O X0^T (X0 X0^T)^-1   (working orientation, m x m)
+    Q = np.linalg.solve(Xw @ Xw.T, Xw @ Ow.T).T
+    qx = np.abs(Q) @ np.abs(Xw)
+    if M_ > N_:
+        qx = qx.T
+    terms = np.abs(W0 * (1 - hp["lr"] * hp["wd"])) + lrs * np.abs(Og)
+    if dtype == torch.bfloat16:
+        Wr_r = torch.from_numpy(Wr).to(torch.bfloat16).double().numpy()
+        ulp = np.maximum(bf16_ulp(Wr_r), bf16_ulp(Wf))
+    else:
+        Wr_r = Wr.astype(np.float32).astype(np.float64)
+        ulp = np.maximum(np.spacing(np.abs(Wr_r).astype(np.float32)),
+                         np.spacing(np.abs(Wf).astype(np.float32))).astype(np.float64)
+    bound = (ulp + lrs * np.abs(Og - Or) * 1.001 + 1.05 * lrs * 2.0 ** -8 * qx
+             + 4 * 2.0 ** -24 * terms)
+    bad = np.abs(Wf - Wr_r) > bound
+    assert not bad.any(), "slice %s: %d params of the step without O beyond the bound" % (
+        key, int(bad.sum()))

@@ -1,15 +1,19 @@
 """GPU parity at the full sizes of the five workloads, in the launch
-configuration the benchmark times (one muon_step over every parameter).
+configuration the benchmark times: one muon_step over every parameter,
+without O outputs (the benchmark's own call, PreparedStep), and beside it
+muon_step_ortho on identical inputs so that O itself meets the oracle.
 
-  * fp32 [24, 1024] and 74 x [24, 10240] (10 steps, teacher-forced: the
-    oracle's step t+1 starts from the GPU's state after step t, so errors do
-    not compound): every slice against the oracle;
-  * stacks + experts, dense layers, MoE model: every slice of the skinny
-    groups, the first and last slice of every other group, against the
-    oracle; the dense [4096, *] groups, whose slices cost the oracle
-    2-4 TFLOP each, are checked on one square slice against the oracle and on
-    every group against the closed form of Newton-Schulz on a Householder-
-    structured input (a property that holds at any size).
+  * fp32 [24, 1024]: every slice against the oracle;
+  * 74 x [24, 10240], 10 steps, teacher-forced (the oracle's step t+1
+    starts from the GPU's state after step t, so errors do not compound):
+    every slice of both calls, every step, element by element;
+  * stacks + experts, MoE model, dense layers: both calls over the whole
+    workload; momentum of the two calls bit for bit, dense-group parameters
+    bit for bit; every slice of the skinny groups and the first and last
+    slice of every other group against the oracle, element by element
+    (the dense layers' [11008, 4096] group is worked on transposed);
+  * every dense group at full size against the closed form of Newton-Schulz
+    on a Householder-structured input (a property that holds at any size).
 """
 import numpy as np
 import pytest
@@ -17,7 +21,7 @@ import torch
 
 import oracle
 import synth
-from helpers import TOL, compare, gpu_step, muon, oracle_step, rel_fro, slices
+from helpers import TOL, compare, compare_folded, gpu_step, muon, oracle_step, slices
 
 pytestmark = pytest.mark.gpu
 
@@ -27,13 +31,6 @@ def hp_of(w):
                 coeffs=w.coeffs)
 
 
-def _check_keys(W0, G, M0, Wd, Md, O, ref, hp, dtype, mode="tc16"):
-    for (p, e), r in ref.items():
-        gp = (slices(Wd[p])[e].cpu(), slices(Md[p])[e].cpu(), slices(O[p])[e].cpu())
-        compare((p, e), gp, r, slices(W0[p])[e].cpu(), slices(G[p])[e].cpu(),
-                slices(M0[p])[e].cpu(), hp, mode, dtype)
-
-
 def test_fp32_24x1024_full():
     w = synth.workload("fp32_24x1024")
     m = muon()
@@ -41,26 +38,51 @@ def test_fp32_24x1024_full():
     plan = m.Plan(list(zip(w.shapes, [w.dtype] * len(w.shapes))))
     Wd = [x.cuda() for x in W]; Md = [x.cuda() for x in M]
     O = gpu_step(plan, Wd, [g.cuda() for g in G], Md, hp_of(w))
-    _check_keys(W, G, M, Wd, Md, O, oracle_step(W, G, M, hp_of(w)), hp_of(w), w.dtype)
+    ref = oracle_step(W, G, M, hp_of(w))
+    for (p, e), r in ref.items():
+        compare((p, e), (Wd[p].cpu(), Md[p].cpu(), O[p].cpu()), r, W[p], G[p], M[p], hp_of(w),
+                "tc16", w.dtype)
 
 
-def test_skinny_74x24x10240_ten_steps_teacher_forced():
+def _both_paths(plan, W, G, M, hp):
+    """The benchmark's call (PreparedStep, no O) on (W, G, M) in place, and
+    muon_step_ortho on copies of W and M.  Returns (W copy, M copy, O)."""
+    m = muon()
+    Wb = [x.clone() for x in W]; Mb = [x.clone() for x in M]
+    O = [torch.empty(x.shape, dtype=torch.float32, device=x.device) for x in W]
+    ws = m.alloc_workspace(plan, W[0].device)
+    m.PreparedStep(plan, W, G, M, workspace=ws, **hp)()
+    torch.cuda.synchronize()
+    assert m.workspace_error(ws) == 0
+    m.step(plan, Wb, G, Mb, workspace=ws, ortho=O, **hp)
+    torch.cuda.synchronize()
+    assert m.workspace_error(ws) == 0
+    del ws
+    return Wb, Mb, O
+
+
+def test_skinny_74x24x10240_ten_steps_bench_call_teacher_forced():
     w = synth.workload("skinny_74x24x10240")
     m = muon()
     hp = hp_of(w)
     plan = m.Plan(list(zip(w.shapes, [w.dtype] * len(w.shapes))))
     Wd = [x.cuda() for x in synth.make_params(w)]
     Md = [x.cuda() for x in synth.make_momentum(w)]
-    ws = m.alloc_workspace(plan)
     for t in range(w.steps):
         G = synth.make_grads(w, t)
         W0 = [x.cpu() for x in Wd]; M0 = [x.cpu() for x in Md]
-        O = gpu_step(plan, Wd, [g.cuda() for g in G], Md, hp, ws=ws)
+        Wb, Mb, O = _both_paths(plan, Wd, [g.cuda() for g in G], Md, hp)
         ref = oracle_step(W0, G, M0, hp)
-        _check_keys(W0, G, M0, Wd, Md, O, ref, hp, w.dtype)
+        for p in range(len(Wd)):
+            assert torch.equal(Md[p], Mb[p]), (t, p)
+            r = ref[(p, 0)]
+            og = O[p].cpu()
+            compare((t, p), (Wb[p].cpu(), Mb[p].cpu(), og), r, W0[p], G[p], M0[p], hp, "tc16",
+                    w.dtype)
+            compare_folded((t, p), Wd[p].cpu(), W0[p], G[p], M0[p], og, r, hp, w.dtype)
 
 
-def _sampled_keys(plan, shapes, skinny_all=True):
+def _sampled_keys(plan, shapes):
     """(param, slice) pairs: all slices of skinny groups, first and last of
     the others."""
     mm = muon()
@@ -72,14 +94,14 @@ def _sampled_keys(plan, shapes, skinny_all=True):
             members[g].append((p, e))
     keys = set()
     for g, lst in members.items():
-        if groups[g]["kernel"] == mm.KERNEL_SKINNY and skinny_all:
+        if groups[g]["kernel"] == mm.KERNEL_SKINNY:
             keys.update(lst)
         else:
             keys.update([lst[0], lst[-1]])
-    return keys, groups, members
+    return keys, groups
 
 
-def _run_workload(name, skip_group=lambda g: False):
+def _run_workload(name, keep=lambda key, group: True):
     w = synth.workload(name)
     m = muon()
     hp = hp_of(w)
@@ -88,24 +110,31 @@ def _run_workload(name, skip_group=lambda g: False):
     W = synth.make_params(w, device="cuda")
     G = synth.make_grads(w, 0, device="cuda")
     M = synth.make_momentum(w, device="cuda")
-    keys, groups, members = _sampled_keys(plan, shapes)
-    keys = {k for k in keys if not skip_group(groups[plan.slice(*k)[0]])}
+    keys, groups = _sampled_keys(plan, shapes)
+    keys = sorted(k for k in keys if keep(k, groups[plan.slice(*k)[0]]))
     W0 = {k: slices(W[k[0]])[k[1]].cpu() for k in keys}
     G0 = {k: slices(G[k[0]])[k[1]].cpu() for k in keys}
     M0 = {k: slices(M[k[0]])[k[1]].cpu() for k in keys}
-    O = gpu_step(plan, W, G, M, hp)
+    Wb, Mb, O = _both_paths(plan, W, G, M, hp)
+    # the two calls: momentum bit for bit; dense-group parameters bit for bit
+    for p in range(len(shapes)):
+        assert torch.equal(M[p], Mb[p]), p
+        if groups[plan.slice(p, 0)[0]]["kernel"] == m.KERNEL_DENSE:
+            assert torch.equal(W[p], Wb[p]), p
     errs = []
     # oracle per group, so one big slice spreads over all host threads
     for g in range(len(groups)):
         ks = [k for k in keys if plan.slice(*k)[0] == g]
         if not ks:
             continue
-        Wl = [W0[k] for k in ks]; Gl = [G0[k] for k in ks]; Ml = [M0[k] for k in ks]
-        ref = oracle_step(Wl, Gl, Ml, hp)
+        ref = oracle_step([W0[k] for k in ks], [G0[k] for k in ks], [M0[k] for k in ks], hp)
         for j, k in enumerate(ks):
-            gp = (slices(W[k[0]])[k[1]].cpu(), slices(M[k[0]])[k[1]].cpu(),
-                  slices(O[k[0]])[k[1]].cpu())
-            compare(k, gp, ref[(j, 0)], W0[k], G0[k], M0[k], hp, "tc16", w.dtype, errs)
+            og = slices(O[k[0]])[k[1]].cpu()
+            compare(k, (slices(Wb[k[0]])[k[1]].cpu(), slices(Mb[k[0]])[k[1]].cpu(), og),
+                    ref[(j, 0)], W0[k], G0[k], M0[k], hp, "tc16", w.dtype, errs)
+            if groups[g]["kernel"] == m.KERNEL_SKINNY:
+                compare_folded(k, slices(W[k[0]])[k[1]].cpu(), W0[k], G0[k], M0[k], og,
+                               ref[(j, 0)], hp, w.dtype)
     return errs
 
 
@@ -119,21 +148,14 @@ def test_moe_model_sampled_slices():
     assert len(errs) == 74 + 2 * 3
 
 
-def test_dense_layers_one_square_slice_against_oracle():
-    # 4096 x 4096 from the dense layer set: a single slice through the whole
-    # step, the oracle spread over the host's threads
-    m = muon()
-    w = synth.workload("dense_24L")
-    hp = hp_of(w)
-    shape = (4096, 4096)
-    W = synth.draw(shape, w.param_std, synth.param_seed(1, 0), w.dtype, "cuda")
-    G = synth.draw(shape, w.grad_std, synth.param_seed(0, 0), w.dtype, "cuda")
-    M = torch.zeros(shape, dtype=torch.float32, device="cuda")
-    W0, G0, M0 = W.cpu(), G.cpu(), M.cpu()
-    plan = m.Plan([(shape, w.dtype)])
-    O = gpu_step(plan, [W], [G], [M], hp)
-    ref = oracle_step([W0], [G0], [M0], hp)
-    compare((0, 0), (W.cpu(), M.cpu(), O[0].cpu()), ref[(0, 0)], W0, G0, M0, hp, "tc16", w.dtype)
+def test_dense_layers_bench_call():
+    # the benchmark's default workload: 24 x {4 x [4096, 4096], [11008, 4096],
+    # 2 x [4096, 11008]}; the oracle takes the first and last slice of the two
+    # [*, 11008] groups (one worked on transposed) and the first [4096, 4096]
+    def keep(key, group):
+        return not (group["M"] == 4096 and group["N"] == 4096 and key[0] != 0)
+    errs = _run_workload("dense_24L", keep)
+    assert len(errs) == 5
 
 
 def _p_scalar(x, T, coeffs):
