@@ -25,7 +25,28 @@
  * Arguments are validated before any launch.  Launch failures return
  * MUON_ERR_CUDA.  A device-side wait that runs out of its iteration budget
  * writes an error word into the workspace header; muon_workspace_error reads
- * it.
+ * it.  Every kernel of a step checks that word when it starts and returns
+ * at once when it is set, and a kernel whose own wait gave up stores no
+ * parameter and no momentum after that point: such a step leaves the
+ * parameters of the slices not yet updated as they were (momenta may have
+ * advanced).  The word stays set until the caller clears it.
+ *
+ * Environment (read by the library at each call):
+ *   MUON_LOG=1        muon_plan prints the plan to stderr (one line per
+ *                     group: dims, dtype, slices, tr, scale, kernel, chunk,
+ *                     workspace).
+ *   MUON_FAULT=alloc  muon_plan fails as if host memory ran out
+ *                     (MUON_ERR_NOMEM), before allocating anything.
+ *   MUON_FAULT=launch the step calls fail as if the first launch had
+ *                     failed (MUON_ERR_CUDA), after validating their
+ *                     arguments and before any device work.
+ *   MUON_FAULT=timeout every bounded device wait of the step kernels gives
+ *                     up at once (budget of zero polls): the step records
+ *                     MUON_ERR_DEVICE_TIMEOUT in the error word; each kernel
+ *                     still waits, with the normal budget, for the copies it
+ *                     has in flight before it returns.
+ * These fault switches exist to test the callers' error paths; unset, they
+ * cost one getenv per call.
  */
 #ifndef MUON_H_
 #define MUON_H_
@@ -51,7 +72,8 @@ typedef enum {
   MUON_ERR_ALIGNMENT = -4,         /* workspace not 256-byte aligned         */
   MUON_ERR_CUDA = -5,              /* a CUDA runtime call failed             */
   MUON_ERR_DEVICE_TIMEOUT = -6,    /* a bounded device wait gave up          */
-  MUON_ERR_WORKSPACE = -7          /* workspace smaller than the plan needs  */
+  MUON_ERR_WORKSPACE = -7,         /* workspace smaller than the plan needs  */
+  MUON_ERR_NOMEM = -8              /* host memory allocation failed          */
 } muon_status;
 
 /* element types of parameters and gradients (momentum is always fp32) */
@@ -89,7 +111,17 @@ typedef struct {
   int skinny_max_m;     /* groups with min(M,N) <= this run on the fused
                            skinny kernel when they fit on chip (default 64,
                            0 or negative disables the skinny kernel)        */
+  int scale_mode;       /* update scale s of a [M, N] slice (the RFC does
+                           not fix it): MUON_SCALE_SQRT_RATIO (default) or
+                           MUON_SCALE_RMS_MATCH                             */
 } muon_options;
+
+/* update scale s in W' = W (1 - lr wd) - lr s O, rounded once to float */
+enum {
+  MUON_SCALE_SQRT_RATIO = 0, /* s = sqrt(max(1, M/N))                          */
+  MUON_SCALE_RMS_MATCH = 1   /* s = 0.2 sqrt(max(M, N)): an update whose RMS is
+                                about 0.2, like a typical AdamW step          */
+};
 
 typedef struct muon_plan_s muon_plan_t;
 
@@ -99,7 +131,7 @@ typedef struct {
   int dtype;
   int count;      /* slices in the group                                   */
   int tr;         /* 1 when M > N: the slice is worked on transposed       */
-  float scale;    /* s = sqrt(max(1, M/N)), rounded once to float          */
+  float scale;    /* update scale s of the options' scale_mode (float)     */
   int kernel;     /* MUON_KERNEL_SKINNY or MUON_KERNEL_DENSE               */
   int cluster;    /* skinny: CTAs per slice (thread-block cluster size)    */
   int chunk;      /* dense: slices per chunk under the workspace cap       */

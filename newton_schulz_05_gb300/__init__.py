@@ -30,6 +30,8 @@ DEFAULT_COEFFS = (3.4445, -4.7750, 2.0315)
 
 _DTYPES = {torch.bfloat16: MUON_BF16, torch.float32: MUON_F32}
 _MODES = {"tc16": MODE_TC16, "fp32": MODE_FP32}
+# update scale s of a [M, N] slice (MUON_SCALE_* in include/muon.h)
+SCALE_MODES = {"sqrt_ratio": 0, "rms_match": 1}
 
 
 class MuonError(RuntimeError):
@@ -44,7 +46,8 @@ class _Shape(ctypes.Structure):
 
 class _Options(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("eps", ctypes.c_float),
-                ("workspace_cap", ctypes.c_size_t), ("skinny_max_m", ctypes.c_int)]
+                ("workspace_cap", ctypes.c_size_t), ("skinny_max_m", ctypes.c_int),
+                ("scale_mode", ctypes.c_int)]
 
 
 class _GroupInfo(ctypes.Structure):
@@ -142,7 +145,8 @@ class Plan:
     """Host-side grouping of parameters by trailing dims (muon_plan)."""
 
     def __init__(self, params: Sequence, mode: str = "tc16", eps: float = 1e-7,
-                 workspace_cap: int = 0, skinny_max_m: int = 64):
+                 workspace_cap: int = 0, skinny_max_m: int = 64,
+                 scale_mode: str = "sqrt_ratio"):
         L = load()
         specs = [_shape_of(p) for p in params]
         n = len(specs)
@@ -158,6 +162,7 @@ class Plan:
         opt.eps = eps
         opt.workspace_cap = workspace_cap
         opt.skinny_max_m = skinny_max_m
+        opt.scale_mode = SCALE_MODES[scale_mode]
         h = ctypes.c_void_p()
         _check(L.muon_plan(arr, n, ctypes.byref(opt), ctypes.byref(h)), "muon_plan")
         self._h = h

@@ -126,6 +126,8 @@ extern "C" muon_status muon_adamw_step(int n, void* const* params, const void* c
   for (int i = 0; i < n; ++i)
     if (!params[i] || !grads[i] || !exp_avg[i] || !exp_avg_sq[i] || numel[i] < 0)
       return MUON_ERR_INVALID_ARG;
+  if (fault_switch() == kFaultLaunch) return MUON_ERR_CUDA;
+  NvtxRange range("muon_adamw_step");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t es = dtype == MUON_BF16 ? 2 : 4;
   AdamwParams p;

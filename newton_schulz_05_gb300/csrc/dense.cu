@@ -65,9 +65,11 @@ template <typename PT>
 __global__ void __launch_bounds__(kNT) front_kernel(
     const __grid_constant__ SlicePtrs ptrs, int64_t m, int64_t n, int64_t m_pad,
     int64_t n_pad, int tr, int vec, float beta, int nesterov, float gscale, const int* skip,
-    char* ws, size_t slice_ws, size_t off_V, size_t off_part) {
+    const int* err, char* ws, size_t slice_ws, size_t off_V, size_t off_part) {
   pdl_wait();
-  if (skip && *skip) return;   // skipped loss-scaled step: momentum untouched
+  // skipped loss-scaled step, or an earlier wait of the step gave up:
+  // momentum untouched
+  if ((skip && *skip) || *err) return;
   const int s = blockIdx.y;
   const int tiles_c = (int)(n_pad / kFrontTileC);
   const int64_t i0 = (int64_t)(blockIdx.x / tiles_c) * kFrontTileR;
@@ -148,8 +150,9 @@ __global__ void __launch_bounds__(kNT) front_kernel(
 
 __global__ void __launch_bounds__(kNT) finalize_kernel(char* ws, size_t slice_ws,
                                                        size_t off_part, size_t off_inv,
-                                                       int nblk, float eps) {
+                                                       int nblk, float eps, const int* err) {
   pdl_wait();
+  if (*err) return;
   char* base = ws + (size_t)blockIdx.x * slice_ws;
   const float* part = reinterpret_cast<const float*>(base + off_part);
   __shared__ float red[kNT / 32];
@@ -164,8 +167,9 @@ template <typename IT>
 __global__ void __launch_bounds__(kNT) normalize_kernel(char* ws, size_t slice_ws,
                                                         size_t off_V, size_t off_X,
                                                         size_t off_inv, int64_t count,
-                                                        int in_place) {
+                                                        int in_place, const int* err) {
   pdl_wait();
+  if (*err) return;
   char* base = ws + (size_t)blockIdx.y * slice_ws;
   float* V = reinterpret_cast<float*>(base + off_V);
   IT* X = reinterpret_cast<IT*>(base + off_X);
@@ -193,9 +197,11 @@ __global__ void __launch_bounds__(kNT) normalize_kernel(char* ws, size_t slice_w
 template <typename PT>
 __global__ void __launch_bounds__(kNT) epilogue_kernel(
     const __grid_constant__ SlicePtrs ptrs, int64_t M, int64_t N, int64_t n_pad, int tr, int vec,
-    float decay, float lr_scale, const int* skip, char* ws, size_t slice_ws, size_t off_O) {
+    float decay, float lr_scale, const int* skip, const int* err, char* ws, size_t slice_ws,
+    size_t off_O) {
   pdl_wait();
-  if (skip && *skip) return;   // skipped loss-scaled step: parameters untouched
+  // skipped loss-scaled step, or a wait of the step gave up: parameters untouched
+  if ((skip && *skip) || *err) return;
   const int s = blockIdx.y;
   const float* O = reinterpret_cast<const float*>(ws + (size_t)s * slice_ws + off_O);
   PT* W = static_cast<PT*>(ptrs.W[s]);
@@ -284,32 +290,40 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   // every launch after the step's first may overlap the previous kernel's
   // tail (programmatic dependent launch; each kernel waits before reading)
   cudaError_t le;
-  if (g.dtype == MUON_BF16)
-    le = launch_k(front_kernel<__nv_bfloat16>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m, g.n,
-                  mp, np, (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip, ws, sws, off.V,
-                  off.part);
-  else
-    le = launch_k(front_kernel<float>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m, g.n, mp, np,
-                  (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip, ws, sws, off.V,
-                  off.part);
+  {
+    NvtxRange r("muon::front_kernel");
+    if (g.dtype == MUON_BF16)
+      le = launch_k(front_kernel<__nv_bfloat16>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m,
+                    g.n, mp, np, (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip,
+                    (const int*)err_word, ws, sws, off.V, off.part);
+    else
+      le = launch_k(front_kernel<float>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m, g.n, mp,
+                    np, (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip,
+                    (const int*)err_word, ws, sws, off.V, off.part);
+  }
   if (le != cudaSuccess) return le;
-  le = launch_k(finalize_kernel, dim3(ns), dim3(kNT), 0, s, true, ws, sws, off.part, off.inv, nblk,
-                st.eps);
+  {
+    NvtxRange r("muon::finalize_kernel");
+    le = launch_k(finalize_kernel, dim3(ns), dim3(kNT), 0, s, true, ws, sws, off.part, off.inv,
+                  nblk, st.eps, (const int*)err_word);
+  }
   if (le != cudaSuccess) return le;
   const int64_t cnt = mp * np;
   int nb = (int)((cnt / 4 + kNT - 1) / kNT);
   if (nb > 1184) nb = 1184;
-  le = launch_k(normalize_kernel<IT>, dim3(nb, ns), dim3(kNT), 0, s, true, ws, sws, off.V, off.X0,
-                off.inv, cnt, st.T == 0 ? 1 : 0);
+  {
+    NvtxRange r("muon::normalize_kernel");
+    le = launch_k(normalize_kernel<IT>, dim3(nb, ns), dim3(kNT), 0, s, true, ws, sws, off.V,
+                  off.X0, off.inv, cnt, st.T == 0 ? 1 : 0, (const int*)err_word);
+  }
   if (le != cudaSuccess) return le;
   size_t xin = off.X0, xout = off.X1;
-  // without O outputs the last product applies the parameter update itself,
-  // for slices stored in the working orientation (a transposed slice would
-  // take a read-modify-write per element in the GEMM epilogue, measured to
-  // stall the tensor pipe: those keep the separate epilogue kernel)
+  // without O outputs the last product applies the parameter update itself
+  // (a transposed slice through a transposing shared-memory tile in the
+  // epilogue, so that its stored rows are read and written in 64-byte pieces)
   bool want_o = false;
   for (int i = 0; i < ns; ++i) want_o = want_o || ptrs.O[i] != nullptr;
-  const bool fuse = sizeof(IT) == 2 && st.T > 0 && !want_o && !g.tr;
+  const bool fuse = sizeof(IT) == 2 && st.T > 0 && !want_o;
   const float decay = 1.f - st.lr * st.wd;
   const float lrs = st.lr * g.scale;
   if constexpr (sizeof(IT) == 2) {
@@ -322,24 +336,34 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
       const bool last = t == st.T - 1;
       TcGemm g1;
       g1.batch = ns; g1.stride = sws; g1.err = err_word; g1.skip = st.skip;
+      g1.wait_limit = st.wait_limit;
       // A = X X^T and A2 = c X X^T + b I (symmetric)
       g1.M = mp; g1.N = mp; g1.K = np;
       g1.A = ws + xin; g1.B = ws + xin; g1.D = ws + off.A; g1.sym = 1;
       g1.D2 = ws + off.A2; g1.alpha2 = st.c; g1.diag2 = st.b;
-      cudaError_t e = tc_gemm(g1, s);
+      cudaError_t e;
+      {
+        NvtxRange r("muon::tc_gemm gram");
+        e = tc_gemm(g1, s);
+      }
       if (e != cudaSuccess) return e;
       // B' = A A2 + a I = b A + c A A + a I (symmetric: A and A2 commute)
       TcGemm g2;
       g2.batch = ns; g2.stride = sws; g2.err = err_word; g2.skip = st.skip;
+      g2.wait_limit = st.wait_limit;
       g2.M = mp; g2.N = mp; g2.K = mp;
       g2.A = ws + off.A; g2.B = ws + off.A2; g2.D = ws + off.B; g2.sym = 1;
       g2.diag = st.a;
-      e = tc_gemm(g2, s);
+      {
+        NvtxRange r("muon::tc_gemm poly");
+        e = tc_gemm(g2, s);
+      }
       if (e != cudaSuccess) return e;
       // X' = B' X, X as an N-major B operand; fp32 O on the last step, or
       // there the update W' = W (1 - lr wd) - lr s O into the parameters
       TcGemm g3;
       g3.batch = ns; g3.stride = sws; g3.err = err_word; g3.skip = st.skip;
+      g3.wait_limit = st.wait_limit;
       g3.M = mp; g3.N = np; g3.K = mp;
       g3.A = ws + off.B; g3.B = ws + xin; g3.b_mn = 1;
       g3.D = ws + (last ? off.V : xout); g3.d_f32 = last ? 1 : 0;
@@ -349,7 +373,10 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
         g3.wm = g.m; g3.wn = g.n; g3.wtr = g.tr;
         g3.decay = decay; g3.lrs = lrs;
       }
-      e = tc_gemm(g3, s);
+      {
+        NvtxRange r("muon::tc_gemm update");
+        e = tc_gemm(g3, s);
+      }
       if (e != cudaSuccess) return e;
       const size_t tmp = xin; xin = xout; xout = tmp;
     }
@@ -388,20 +415,22 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   const int tiles = (!g.tr && vec) ? (int)(((g.M + 31) / 32) * ((g.N + 127) / 128))
                                    : (int)(((g.M + 31) / 32) * ((g.N + 31) / 32));
   if (fuse) return cudaSuccess;   // the last product updated the parameters
+  NvtxRange r("muon::epilogue_kernel");
   if (g.dtype == MUON_BF16)
     return launch_k(epilogue_kernel<__nv_bfloat16>, dim3(tiles, ns), dim3(kNT), 0, s, true, ptrs,
-                    g.M, g.N, np, (int)g.tr, vec, decay, lrs, st.skip, ws, sws, off.V);
+                    g.M, g.N, np, (int)g.tr, vec, decay, lrs, st.skip, (const int*)err_word, ws,
+                    sws, off.V);
   return launch_k(epilogue_kernel<float>, dim3(tiles, ns), dim3(kNT), 0, s, true, ptrs, g.M, g.N,
-                  np, (int)g.tr, vec, decay, lrs, st.skip, ws, sws, off.V);
+                  np, (int)g.tr, vec, decay, lrs, st.skip, (const int*)err_word, ws, sws, off.V);
 }
 
 }  // namespace
 
 // front, finalize, normalize, 3 products per NS step, epilogue; in the
-// tensor-core mode the last product applies the update to slices that are
-// not transposed (no epilogue launch)
+// tensor-core mode the last product applies the update (no epilogue launch)
 int dense_launches(int ns_steps, int mode, int tr) {
-  return (mode == MUON_MODE_TC16 && ns_steps > 0 && !tr ? 3 : 4) + 3 * ns_steps;
+  (void)tr;
+  return (mode == MUON_MODE_TC16 && ns_steps > 0 ? 3 : 4) + 3 * ns_steps;
 }
 
 namespace {

@@ -7,6 +7,7 @@
 #include <vector>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "muon.h"
 
@@ -20,6 +21,22 @@ constexpr int kFrontTileC = 128;
 
 // device error codes written into the workspace header
 constexpr int kDevErrTimeout = 1;
+// polls of an mbarrier before a bounded wait gives up (about a second or
+// more); waits for a kernel's own copies in flight always use this budget
+constexpr uint32_t kWaitLimit = 1u << 26;
+
+// NVTX range over a scope (a step, a kernel launch): shows up in Nsight
+// timelines; without a tool attached it costs a few nanoseconds
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// MUON_FAULT switch of this call: 0 none, else one of the kFault* values
+enum { kFaultNone = 0, kFaultAlloc = 1, kFaultLaunch = 2, kFaultTimeout = 3 };
+int fault_switch();
 
 struct Group {
   int64_t M = 0, N = 0, m = 0, n = 0;
@@ -70,6 +87,7 @@ struct StepArgs {
   float eps;
   float gscale = 1.f;          // gradients are multiplied by this (1/loss scale)
   const int* skip = nullptr;   // device flag: when set, the step changes nothing
+  uint32_t wait_limit = kWaitLimit;   // polls of a bounded wait on the main path
 };
 
 size_t dense_slice_ws(const Group& g, int mode);

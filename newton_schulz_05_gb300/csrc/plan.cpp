@@ -8,6 +8,8 @@
 // The plan is built once, on the host, with no device call.
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <queue>
@@ -16,6 +18,27 @@
 #include "internal.h"
 
 namespace muon {
+
+int fault_switch() {
+  const char* f = std::getenv("MUON_FAULT");
+  if (!f || !*f) return kFaultNone;
+  if (!std::strcmp(f, "alloc")) return kFaultAlloc;
+  if (!std::strcmp(f, "launch")) return kFaultLaunch;
+  if (!std::strcmp(f, "timeout")) return kFaultTimeout;
+  return kFaultNone;
+}
+
+static bool log_enabled() {
+  const char* v = std::getenv("MUON_LOG");
+  return v && *v && std::strcmp(v, "0") != 0;
+}
+
+// update scale of a [M, N] slice, rounded once to float
+static float update_scale(int64_t M, int64_t N, int mode) {
+  if (mode == MUON_SCALE_RMS_MATCH) return (float)(0.2 * std::sqrt((double)(M > N ? M : N)));
+  const double ratio = (double)M / (double)N;
+  return (float)std::sqrt(ratio > 1.0 ? ratio : 1.0);
+}
 
 static int64_t round_up(int64_t x, int64_t k) { return (x + k - 1) / k * k; }
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -71,6 +94,7 @@ void muon_options_default(muon_options* o) {
   o->eps = 1e-7f;
   o->workspace_cap = 0;
   o->skinny_max_m = 64;
+  o->scale_mode = MUON_SCALE_SQRT_RATIO;
 }
 
 muon_status muon_plan(const muon_shape* shapes, int n, const muon_options* opt,
@@ -82,9 +106,13 @@ muon_status muon_plan(const muon_shape* shapes, int n, const muon_options* opt,
   if (opt) o = *opt;
   if (o.mode != MUON_MODE_TC16 && o.mode != MUON_MODE_FP32) return MUON_ERR_INVALID_ARG;
   if (!(o.eps >= 0.f)) return MUON_ERR_INVALID_ARG;
+  if (o.scale_mode != MUON_SCALE_SQRT_RATIO && o.scale_mode != MUON_SCALE_RMS_MATCH)
+    return MUON_ERR_INVALID_ARG;
+  if (fault_switch() == kFaultAlloc) return MUON_ERR_NOMEM;
 
   muon_plan_s* P = new (std::nothrow) muon_plan_s();
-  if (!P) return MUON_ERR_INVALID_ARG;
+  if (!P) return MUON_ERR_NOMEM;
+  try {
   P->opt = o;
   P->shapes.assign(shapes, shapes + n);
   int slice = 0;
@@ -110,8 +138,7 @@ muon_status muon_plan(const muon_shape* shapes, int n, const muon_options* opt,
       G.tr = M > N ? 1 : 0;
       G.m = G.tr ? N : M;
       G.n = G.tr ? M : N;
-      const double ratio = (double)M / (double)N;
-      G.scale = (float)std::sqrt(ratio > 1.0 ? ratio : 1.0);
+      G.scale = update_scale(M, N, o.scale_mode);
       P->groups.push_back(G);
       g = (int)P->groups.size() - 1;
     }
@@ -147,6 +174,30 @@ muon_status muon_plan(const muon_shape* shapes, int n, const muon_options* opt,
     if (need > ws) ws = need;
   }
   P->ws_bytes = kHeaderBytes + ws;
+  } catch (const std::bad_alloc&) {
+    delete P;
+    return MUON_ERR_NOMEM;
+  }
+  if (log_enabled()) {
+    std::fprintf(stderr, "muon_plan: %d parameters, %d slices, %d groups, workspace %zu bytes\n",
+                 n, (int)P->slice_group.size(), (int)P->groups.size(), P->ws_bytes);
+    for (size_t k = 0; k < P->groups.size(); ++k) {
+      const Group& G = P->groups[k];
+      if (G.kernel == MUON_KERNEL_SKINNY)
+        std::fprintf(stderr,
+                     "muon_plan: group %zu [%lld,%lld] %s slices=%d m=%lld n=%lld tr=%d scale=%.9g "
+                     "kernel=skinny cluster=%d\n",
+                     k, (long long)G.M, (long long)G.N, G.dtype == MUON_BF16 ? "bf16" : "f32",
+                     G.count(), (long long)G.m, (long long)G.n, G.tr, (double)G.scale, G.cluster);
+      else
+        std::fprintf(stderr,
+                     "muon_plan: group %zu [%lld,%lld] %s slices=%d m=%lld n=%lld tr=%d scale=%.9g "
+                     "kernel=dense chunk=%d slice_workspace=%zu\n",
+                     k, (long long)G.M, (long long)G.N, G.dtype == MUON_BF16 ? "bf16" : "f32",
+                     G.count(), (long long)G.m, (long long)G.n, G.tr, (double)G.scale, G.chunk,
+                     G.slice_ws);
+    }
+  }
   *out = P;
   return MUON_OK;
 }
@@ -264,6 +315,7 @@ const char* muon_status_string(muon_status s) {
     case MUON_ERR_CUDA: return "CUDA runtime error";
     case MUON_ERR_DEVICE_TIMEOUT: return "device wait ran out of its budget";
     case MUON_ERR_WORKSPACE: return "workspace too small for the plan";
+    case MUON_ERR_NOMEM: return "host memory allocation failed";
   }
   return "unknown status";
 }

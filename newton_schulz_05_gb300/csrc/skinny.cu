@@ -111,10 +111,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
-// bounded wait for the phase of parity `parity`; false when the budget ran out
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// bounded wait for the phase of parity `parity`: at most `limit` polls
+// (zero: give up at once); false when the budget ran out
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t limit = kWaitLimit) {
   const uint32_t a = smem_u32(bar);
-  for (uint32_t i = 0; i < (1u << 26); ++i) {
+  for (uint32_t i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -441,7 +443,11 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   const int c_lo = jc0 * 32, c_hi = min(p.n, jc1 * 32);
   const int nstage = jc1 > jc0 ? (c_hi - c_lo + S::SW - 1) / S::SW : 0;   // pass-1 stages
   const int nstage_w = (nstage + 1) / 2;                                      // pass-2 stages
-  bool wait_ok = true;
+  // live: this thread stores results.  Cleared when one of its waits gave
+  // up, or when the error word was set (by an earlier kernel of the step or
+  // another cluster); the control flow, the cluster syncs and the waits for
+  // copies in flight stay the same, only the stores stop.
+  bool live = *static_cast<volatile int*>(p.err) == 0;
   // Rows [part*R, (part+1)*R) of stage k of pass `w2` (0: G and M rows,
   // columns [c_lo + k*SW, ...); 1: W rows, columns [c_lo + 2k*SW, ...)); one
   // warp issues them, one row per lane.  Part 0 posts the stage's byte count (copies of other parts may
@@ -484,9 +490,12 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
   auto stage_wait = [&](int k, int w2) {
     uint64_t* bar = w2 ? &full_w[k % NSTW] : &full[k % NSTG];
     const uint32_t par = (uint32_t)((k / (w2 ? NSTW : NSTG)) & 1);
-    if (!mbar_wait(bar, par) && wait_ok) {
-      wait_ok = false;
-      atomicExch(p.err, kDevErrTimeout);
+    if (!mbar_wait(bar, par, st.wait_limit)) {
+      if (live) atomicExch(p.err, kDevErrTimeout);
+      live = false;
+      // the stage's copies are still owed to this buffer: wait for them
+      // with the normal budget before it is read or refilled
+      mbar_wait(bar, par);
     }
   };
   // L2 prefetch of one superchunk's gradient and momentum rows (direct path)
@@ -588,10 +597,10 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
         }
         if (staged) {
           const int c = cb + h * 16 + 4 * t4;
-          if (row_ok(rb) && c < p.n)
+          if (live && row_ok(rb) && c < p.n)
             *reinterpret_cast<float4*>(mo_row[rb] + c) =
                 make_float4(mv[rb][h][0], mv[rb][h][1], mv[rb][h][2], mv[rb][h][3]);
-        } else {
+        } else if (live) {
           acc_.store_f32(Mo, rb * 8 + g, cb + h * 16 + 4 * t4, mv[rb][h]);
         }
         xr[rb][2 * h] = pack_bf16(vv[0], vv[1]);
@@ -740,6 +749,9 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
     }
 
   // ---- pass 2: O = Q X_0 and W' = W (1 - lr wd) - lr s O -------------------------
+  // a wait that gave up anywhere before the cluster sync (this cluster's
+  // reduction included) leaves every parameter untouched
+  live = live && *static_cast<volatile int*>(p.err) == 0;
   float wbuf[MB][2][4];
   auto load_w = [&](int q) {
     const int cb = sc_col(q);
@@ -840,7 +852,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
         #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int c = cb + h * 16 + 4 * t4;
-          if (row_ok(rb) && c < p.n) {
+          if (live && row_ok(rb) && c < p.n) {
             float wn[4];
             wn[0] = fmaf(wcur[rb][h][0], p.decay, o[rb][2 * h][0]);
             wn[1] = fmaf(wcur[rb][h][1], p.decay, o[rb][2 * h][1]);
@@ -870,7 +882,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
         #pragma unroll
         for (int e = 0; e < 4; ++e) wn[e] = fmaf(wcur[rb][h][e], p.decay, -p.lrs * ov[e]);
         if (staged) {
-          if (row_ok(rb) && c < p.n) {
+          if (live && row_ok(rb) && c < p.n) {
             PT* wp = W + (mo_row[rb] - Mo) + c;     // same row offset as the momentum
             if constexpr (sizeof(PT) == 2) {
               uint2 u;
@@ -883,7 +895,7 @@ __global__ void __launch_bounds__(NW * 32, 1) skinny_kernel(const __grid_constan
             if (Oout)
               *reinterpret_cast<float4*>(Oout + (mo_row[rb] - Mo) + c) = make_float4(ov[0], ov[1], ov[2], ov[3]);
           }
-        } else {
+        } else if (live) {
           acc_.store(W, i, c, wn);
           if (Oout) acc_.store_f32(Oout, i, c, ov);
         }

@@ -18,6 +18,7 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
                       void* stream, float* const* ortho, float inv_scale = 1.f,
                       int* found_inf = nullptr) {
   if (!P) return MUON_ERR_INVALID_ARG;
+  NvtxRange range(found_inf ? "muon_step_amp" : ortho ? "muon_step_ortho" : "muon_step");
   const int np = (int)P->shapes.size();
   if (np > 0 && (!params || !grads || !momentum)) return MUON_ERR_INVALID_ARG;
   for (int p = 0; p < np; ++p)
@@ -38,6 +39,9 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
   if (!std::isfinite(inv_scale)) return MUON_ERR_INVALID_ARG;
   st.gscale = inv_scale;
   st.skip = found_inf;
+  const int fault = fault_switch();
+  if (fault == kFaultLaunch) return MUON_ERR_CUDA;
+  if (fault == kFaultTimeout) st.wait_limit = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   int* err_word = reinterpret_cast<int*>(ws);
@@ -76,10 +80,12 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
       const int ns = cnt - c0 < per ? cnt - c0 : per;
       fill(g, c0, ns);
       cudaError_t e;
-      if (g.kernel == MUON_KERNEL_SKINNY)
+      if (g.kernel == MUON_KERNEL_SKINNY) {
+        NvtxRange r("muon::skinny_kernel");
         e = launch_skinny(g, ptrs, ns, st, err_word, s);
-      else
+      } else {
         e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body, err_word, s, !first);
+      }
       if (e != cudaSuccess) return MUON_ERR_CUDA;
       first = false;
     }

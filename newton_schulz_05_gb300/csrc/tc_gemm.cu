@@ -41,7 +41,6 @@ constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int NTHREADS = 192;
 constexpr int EPI_BYTES = 8192;                 // staging bytes per epilogue warp
-constexpr uint32_t kWaitLimit = 1u << 26;       // try_wait polls before giving up
 
 struct TcParams {
   int M, N, K;
@@ -56,48 +55,77 @@ struct TcParams {
   uint32_t idesc128;   // M = 128, N = 128: tiles with one 128-column half to compute
   int* err;
   const int* skip;
+  uint32_t wait_limit;   // polls of a wait on the main path (drains: kWaitLimit)
   // fused parameter update (last product of the step): the epilogue applies
   // W' = W decay - lrs O to the parameter slices instead of storing O
   int fuse;
   int w_f32;           // parameter dtype fp32 (else bf16)
   int wm, wn;          // working dims of a slice (m rows of O, n columns)
   int wtr;             // the parameter is stored transposed ([n, m])
-  int wvec;            // rows of every slice start 16-byte aligned (not wtr)
+  int wvec;            // rows of every slice start 16-byte aligned (stored rows)
   float decay, lrs;
   void* W[kMaxSlicesPerLaunch];
 };
 
-// W' = W decay - lrs O for the 32 outputs o[] of working row r, columns
-// [c0, c0 + 32) of slice W (stored [m, n], or [n, m] when transposed)
+// W' = W decay - lrs O on `cnt` consecutive stored elements row[0..cnt) with
+// their O values o[0..cnt); 16-byte accesses when vec and cnt == 32
 template <typename PT>
-__device__ __forceinline__ void fused_update(const TcParams& p, PT* W, int r, int c0, const float* o) {
-  if (r >= p.wm) return;   // padding row
-  if (!p.wtr) {
-    PT* row = W + (size_t)r * p.wn + c0;
-    if (p.wvec && c0 + 32 <= p.wn) {
-      constexpr int E = 16 / sizeof(PT);   // elements per 16-byte access
+__device__ __forceinline__ void update_run(const TcParams& p, PT* row, const float* o, int cnt,
+                                           bool vec) {
+  if (vec && cnt == 32) {
+    constexpr int E = 16 / sizeof(PT);   // elements per 16-byte access
+    #pragma unroll
+    for (int k = 0; k < 32 / E; ++k) {
+      uint4 u = reinterpret_cast<const uint4*>(row)[k];
+      PT* e = reinterpret_cast<PT*>(&u);
       #pragma unroll
-      for (int k = 0; k < 32 / E; ++k) {
-        uint4 u = reinterpret_cast<const uint4*>(row)[k];
-        PT* e = reinterpret_cast<PT*>(&u);
-        #pragma unroll
-        for (int i = 0; i < E; ++i) e[i] = from_f<PT>(fmaf(to_f(e[i]), p.decay, -p.lrs * o[k * E + i]));
-        reinterpret_cast<uint4*>(row)[k] = u;
-      }
-    } else {
-      #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < p.wn) row[j] = from_f<PT>(fmaf(to_f(row[j]), p.decay, -p.lrs * o[j]));
+      for (int i = 0; i < E; ++i) e[i] = from_f<PT>(fmaf(to_f(e[i]), p.decay, -p.lrs * o[k * E + i]));
+      reinterpret_cast<uint4*>(row)[k] = u;
     }
   } else {
-    // stored element (c, r): consecutive lanes (rows r) touch consecutive addresses
     #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (c0 + j < p.wn) {
-        PT* w = W + (size_t)(c0 + j) * p.wm + r;
-        *w = from_f<PT>(fmaf(to_f(*w), p.decay, -p.lrs * o[j]));
-      }
+      if (j < cnt) row[j] = from_f<PT>(fmaf(to_f(row[j]), p.decay, -p.lrs * o[j]));
   }
+}
+
+constexpr int kTrPitch = 36;   // floats per row of the transposing tile (16-byte rows)
+
+// W' = W decay - lrs O for the 32 x 32 outputs of working rows
+// [row0, row0 + 32) (lane = row), columns [c0, c0 + 32) (o[] per lane) of
+// slice W, stored [m, n], or [n, m] when transposed.  A transposed slice
+// goes through a shared-memory tile (32 x kTrPitch floats, `tile`): lane j
+// then updates stored row c0 + j, whose 32 elements of columns
+// [row0, row0 + 32) are contiguous, so both orientations touch the
+// parameters in 64-byte row pieces.  Called by all lanes of the warp.
+template <typename PT>
+__device__ __forceinline__ void fused_update(const TcParams& p, PT* W, int row0, int c0,
+                                             float* o, float* tile) {
+  const int lane = threadIdx.x & 31;
+  if (!p.wtr) {
+    const int r = row0 + lane;
+    if (r < p.wm && c0 < p.wn) {
+      const int cnt = p.wn - c0 < 32 ? p.wn - c0 : 32;
+      update_run<PT>(p, W + (size_t)r * p.wn + c0, o, cnt, p.wvec != 0);
+    }
+    return;
+  }
+  // tile[j][i] = O(working row row0 + i, working column c0 + j)
+  #pragma unroll
+  for (int j = 0; j < 32; ++j) tile[j * kTrPitch + lane] = o[j];
+  __syncwarp();
+  const int k = c0 + lane;   // stored row
+  if (k < p.wn && row0 < p.wm) {
+    float t[32];
+    #pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 x = reinterpret_cast<const float4*>(tile + lane * kTrPitch)[q];
+      t[4 * q] = x.x; t[4 * q + 1] = x.y; t[4 * q + 2] = x.z; t[4 * q + 3] = x.w;
+    }
+    const int cnt = p.wm - row0 < 32 ? p.wm - row0 : 32;
+    update_run<PT>(p, W + (size_t)k * p.wm + row0, t, cnt, p.wvec != 0);
+  }
+  __syncwarp();   // the tile is rewritten by the next chunk
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -115,10 +143,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
-// bounded wait for the phase of parity `parity` to complete
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// bounded wait for the phase of parity `parity` to complete: at most
+// `limit` polls (zero: give up at once)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t limit = kWaitLimit) {
   const uint32_t a = smem_u32(bar);
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+  for (uint32_t i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -279,13 +309,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* mdrain = tempty + 2;    // completion of every MMA this CTA issued
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdrain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    mbar_init(mdrain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -304,8 +336,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // launched as a dependent of the previous kernel: the setup above overlaps
   // its tail; nothing global is touched before it has completed
   pdl_wait();
-  // a skipped loss-scaled step computes nothing
-  const bool skipped = p.skip && *p.skip;
+  // a skipped loss-scaled step computes nothing, nor does a step in which
+  // an earlier kernel's wait gave up
+  const bool skipped = (p.skip && *p.skip) || *static_cast<volatile int*>(p.err) != 0;
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -323,7 +356,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&empty[s], ph ^ 1)) { fail(); break; }
+          if (!mbar_wait(&empty[s], ph ^ 1, p.wait_limit)) { fail(); break; }
           unsigned char* sa = smem + s * STAGE_BYTES;
           unsigned char* sb = sa + A_BYTES;
           mbar_expect_tx(&full[s], STAGE_BYTES);
@@ -354,14 +387,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int n_hi = J * BN + BN > p.N ? p.N - J * BN : BN;
         const uint32_t idesc = n_hi - n_lo == BN ? p.idesc : p.idesc128;
         const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], aph ^ 1)) { fail(); break; }
+        if (!mbar_wait(&tempty[acc], aph ^ 1, p.wait_limit)) { fail(); break; }
         tc_fence_after();
         const uint32_t dt = tmem + acc * BN + n_lo;
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&full[s], ph)) { fail(); ok = false; break; }
+          if (!mbar_wait(&full[s], ph, p.wait_limit)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
           // K-major B: row n_lo of the tile starts n_lo * 128 bytes in (a
@@ -379,6 +412,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!ok) break;
         mma_commit(&tfull[acc]);
       }
+      // every MMA issued above completes before the teardown releases the
+      // tensor memory (on a wait that gave up, no epilogue may have waited)
+      if (it > 0) {
+        mma_commit(mdrain);
+        if (!mbar_wait(mdrain, 0)) fail();
+      }
     }
   } else {
     // epilogue warps 2..5: TMEM lane quarter q = warp % 4, 32 rows each
@@ -393,7 +432,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int b, I, J;
       tile_coords(p, t, b, I, J);
       const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], aph)) { fail(); break; }
+      if (!mbar_wait(&tfull[acc], aph, p.wait_limit)) { fail(); break; }
       tc_fence_after();
       const int row0 = I * BM + q * 32;
       const int row = row0 + lane;
@@ -414,8 +453,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           v[j] = fmaf(p.alpha, v[j], d * p.diag);
         }
         if (p.fuse) {
-          if (p.w_f32) fused_update<float>(p, static_cast<float*>(p.W[b]), row, col0, v);
-          else fused_update<__nv_bfloat16>(p, static_cast<__nv_bfloat16*>(p.W[b]), row, col0, v);
+          float* tile = reinterpret_cast<float*>(epi + q * EPI_BYTES);
+          if (p.w_f32) fused_update<float>(p, static_cast<float*>(p.W[b]), row0, col0, v, tile);
+          else fused_update<__nv_bfloat16>(p, static_cast<__nv_bfloat16*>(p.W[b]), row0, col0, v, tile);
           continue;
         }
         // the staging buffer of this chunk is free once the stores issued from
@@ -566,9 +606,11 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
     if (g.batch > kMaxSlicesPerLaunch || g.sym || g.D2) return cudaErrorInvalidValue;
     p.w_f32 = g.w_f32; p.wm = (int)g.wm; p.wn = (int)g.wn; p.wtr = g.wtr;
     p.decay = g.decay; p.lrs = g.lrs;
-    int vec = g.wtr ? 0 : 1;
+    // 16-byte accesses along stored rows: wn (or wm when transposed)
+    // elements per stored row
+    int vec = 1;
     const size_t es = g.w_f32 ? 4 : 2;
-    if ((size_t)g.wn * es % 16) vec = 0;
+    if ((size_t)(g.wtr ? g.wm : g.wn) * es % 16) vec = 0;
     for (int i = 0; i < g.batch; ++i) {
       p.W[i] = g.W[i];
       if (reinterpret_cast<uintptr_t>(g.W[i]) % 16) vec = 0;
@@ -582,6 +624,7 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
   p.idesc128 = tc_idesc_f16(BM, 128, g.b_mn);
   p.err = g.err;
   p.skip = g.skip;
+  p.wait_limit = g.wait_limit;
   const size_t smem = tc_gemm_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);

@@ -40,8 +40,10 @@ struct TcGemm {
   int w_f32 = 0, wtr = 0;
   int64_t wm = 0, wn = 0;
   float decay = 1.f, lrs = 0.f;
-  int* err = nullptr;   // device error word (bounded waits)
+  int* err = nullptr;   // device error word (bounded waits); when set at the
+                        // kernel's start, the kernel returns at once
   const int* skip = nullptr;  // device flag: when set, the kernel returns at once
+  uint32_t wait_limit = 1u << 26;   // polls of a main-path wait before giving up
 };
 
 cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s);

@@ -63,7 +63,7 @@ def lib():
         L = ctypes.CDLL(path)
         L.oracle_plan.restype = ctypes.c_int
         L.oracle_plan.argtypes = [ctypes.c_int, _ip, _i64p, _ip, _ip, _ip, ctypes.c_int,
-                                  _i64p, _i64p, _ip, _ip, _ip, _fp]
+                                  _i64p, _i64p, _ip, _ip, _ip, _fp, ctypes.c_int]
         L.oracle_momentum.argtypes = [ctypes.c_int64, _dp, _dp, ctypes.c_double, ctypes.c_int, _dp, _dp]
         L.oracle_normalize.argtypes = [ctypes.c_int64, _dp, ctypes.c_double, _dp]
         L.oracle_newton_schulz.argtypes = [ctypes.c_int64, ctypes.c_int64, _dp, ctypes.c_int,
@@ -105,11 +105,15 @@ def _ptr(a: np.ndarray):
 
 # --------------------------------------------------------------------------
 # plan
-def plan(shapes: Sequence[Tuple[int, ...]], dtypes: Sequence[str]):
+SCALE_MODES = {"sqrt_ratio": 0, "rms_match": 1}
+
+
+def plan(shapes: Sequence[Tuple[int, ...]], dtypes: Sequence[str], scale_mode: str = "sqrt_ratio"):
     """Group slices by (M, N, dtype) in order of first appearance.
 
     Returns (slice_group, slice_index, groups) with groups a list of dicts
-    {M, N, dtype, count, tr, scale(float32)}."""
+    {M, N, dtype, count, tr, scale(float32)}; scale_mode "sqrt_ratio" gives
+    s = sqrt(max(1, M/N)), "rms_match" s = 0.2 sqrt(max(M, N))."""
     n = len(shapes)
     ndim = (ctypes.c_int * max(n, 1))()
     dims = (ctypes.c_int64 * max(3 * n, 1))()
@@ -127,7 +131,8 @@ def plan(shapes: Sequence[Tuple[int, ...]], dtypes: Sequence[str]):
     gM = (ctypes.c_int64 * cap)(); gN = (ctypes.c_int64 * cap)()
     gd = (ctypes.c_int * cap)(); gc = (ctypes.c_int * cap)(); gt = (ctypes.c_int * cap)()
     gs = (ctypes.c_float * cap)()
-    r = lib().oracle_plan(n, ndim, dims, dt, sg, si, cap, gM, gN, gd, gc, gt, gs)
+    r = lib().oracle_plan(n, ndim, dims, dt, sg, si, cap, gM, gN, gd, gc, gt, gs,
+                          SCALE_MODES[scale_mode])
     if r < 0:
         raise ValueError("oracle_plan rejected the shapes (code %d)" % r)
     inv = {v: k for k, v in DTYPE_CODES.items()}

@@ -76,8 +76,11 @@ extern "C" {
 // Parameters are walked in call order, slices e = 0..E-1 inside each.  The
 // key is (M, N, dtype); groups are numbered by the first appearance of their
 // key; a slice's index inside its group is its order of encounter.  A 2D
-// parameter is a one-slice stack.  tr = (M > N); s = sqrt(max(1, M/N)),
-// rounded once to float.
+// parameter is a one-slice stack.  tr = (M > N).  The update scale s (the
+// RFC leaves it open) is, rounded once to float,
+//   scale_mode 0: s = sqrt(max(1, M/N));
+//   scale_mode 1: s = 0.2 * sqrt(max(M, N)) (an update of RMS 0.2 when O has
+//                 unit singular values).
 //
 // dims: 3 entries per parameter (unused ones ignored); ndim in {2, 3}.
 // Outputs per slice (in walk order): slice_group, slice_index.
@@ -88,7 +91,7 @@ int oracle_plan(int nparams, const int* ndim, const int64_t* dims,
                 const int* dtype, int* slice_group, int* slice_index,
                 int max_groups, int64_t* group_M, int64_t* group_N,
                 int* group_dtype, int* group_count, int* group_tr,
-                float* group_scale) {
+                float* group_scale, int scale_mode) {
   int ngroups = 0;
   int64_t s = 0;
   for (int p = 0; p < nparams; ++p) {
@@ -106,8 +109,12 @@ int oracle_plan(int nparams, const int* ndim, const int64_t* dims,
       group_M[g] = M; group_N[g] = N; group_dtype[g] = dtype[p];
       group_count[g] = 0;
       group_tr[g] = M > N ? 1 : 0;
-      double ratio = (double)M / (double)N;
-      group_scale[g] = (float)std::sqrt(ratio > 1.0 ? ratio : 1.0);
+      if (scale_mode == 1) {
+        group_scale[g] = (float)(0.2 * std::sqrt((double)(M > N ? M : N)));
+      } else {
+        double ratio = (double)M / (double)N;
+        group_scale[g] = (float)std::sqrt(ratio > 1.0 ? ratio : 1.0);
+      }
     }
     for (int64_t e = 0; e < E; ++e, ++s) {
       slice_group[s] = g;

@@ -1,8 +1,11 @@
 /* The C ABI of libmuon used from plain C (no Python, no CUDA headers): plan a
- * parameter set, query groups and slices, assign slices to replicas, and
- * check the argument errors, all host-only calls.  Prints "ok" and exits 0
+ * parameter set, query groups and slices, assign slices to replicas, check
+ * the argument errors and the host-side fault switches, all host-only calls.  Prints "ok" and exits 0
  * when every check holds; otherwise prints the failed check and exits 1. */
+#define _POSIX_C_SOURCE 200112L
+#include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "muon.h"
@@ -40,7 +43,8 @@ int main(void) {
 
   muon_options opt;
   muon_options_default(&opt);
-  CHECK(opt.mode == MUON_MODE_TC16 && opt.skinny_max_m == 64);
+  CHECK(opt.mode == MUON_MODE_TC16 && opt.skinny_max_m == 64 &&
+        opt.scale_mode == MUON_SCALE_SQRT_RATIO);
 
   muon_plan_t* plan = NULL;
   CHECK(muon_plan(shapes, 76, &opt, &plan) == MUON_OK && plan != NULL);
@@ -62,8 +66,38 @@ int main(void) {
   int launches = 0;
   /* one fused launch for the skinny group; per dense group front, finalize,
    * normalize and three products per step, the last of which applies the
-   * update, plus an epilogue launch for the transposed group */
-  CHECK(muon_plan_launches(plan, 5, &launches) == MUON_OK && launches == 1 + 18 + 19);
+   * update (transposed groups too) */
+  CHECK(muon_plan_launches(plan, 5, &launches) == MUON_OK && launches == 1 + 18 + 18);
+
+  /* the other update scale: s = 0.2 sqrt(max(M, N)) */
+  muon_options opt2 = opt;
+  opt2.scale_mode = MUON_SCALE_RMS_MATCH;
+  muon_plan_t* plan2 = NULL;
+  CHECK(muon_plan(shapes, 76, &opt2, &plan2) == MUON_OK && plan2 != NULL);
+  CHECK(muon_plan_group(plan2, 0, &gi) == MUON_OK &&
+        gi.scale == (float)(0.2 * 101.19288512538813) /* sqrt(10240) */);
+  CHECK(muon_plan_group(plan2, 2, &gi) == MUON_OK &&
+        gi.scale == (float)(0.2 * 45.254833995939045) /* sqrt(2048) */);
+  muon_plan_destroy(plan2);
+  opt2.scale_mode = 7;
+  CHECK(muon_plan(shapes, 76, &opt2, &plan2) == MUON_ERR_INVALID_ARG);
+
+  /* host-side fault switches: status codes, no device work */
+  setenv("MUON_FAULT", "alloc", 1);
+  plan2 = NULL;
+  CHECK(muon_plan(shapes, 76, &opt, &plan2) == MUON_ERR_NOMEM && plan2 == NULL);
+  setenv("MUON_FAULT", "launch", 1);
+  {
+    void* fake[76];
+    float* fakef[76];
+    for (int i = 0; i < 76; ++i) {
+      fake[i] = (void*)(uintptr_t)(0x10000 + 256 * i);
+      fakef[i] = (float*)fake[i];
+    }
+    CHECK(muon_step(plan, fake, (const void* const*)fake, fakef, 0.02f, 0.95f, 0.1f, 1, 5, NULL,
+                    (void*)(uintptr_t)0x100000, ws, NULL) == MUON_ERR_CUDA);
+  }
+  unsetenv("MUON_FAULT");
 
   /* replicas: every slice has one owner, the loads sum up */
   int owner[78];
@@ -85,6 +119,7 @@ int main(void) {
         MUON_ERR_INVALID_ARG);
   CHECK(muon_plan_partition(plan, 0, 5, 1.0, 1.0, owner, NULL) == MUON_ERR_INVALID_ARG);
   CHECK(strcmp(muon_status_string(MUON_ERR_WORKSPACE), "workspace too small for the plan") == 0);
+  CHECK(strcmp(muon_status_string(MUON_ERR_NOMEM), "host memory allocation failed") == 0);
 
   muon_plan_destroy(plan);
   if (fails) return 1;

@@ -62,6 +62,13 @@ def gpu_step(plan, W, G, M, hp, ortho=True, ws=None):
     return O
 
 
+def update_scale(M, N, hp):
+    """Update scale s of a [M, N] slice (float32 value), by hp's scale_mode."""
+    if hp.get("scale_mode", "sqrt_ratio") == "rms_match":
+        return float(np.float32(0.2 * np.sqrt(max(M, N))))
+    return float(np.float32(np.sqrt(max(1.0, M / N))))
+
+
 def oracle_step(W, G, M, hp, which=None):
     """fp64 oracle over the slices of W/G/M (CPU tensors).  `which` selects
     (param, slice) pairs; default all.  Returns {(p, e): (W', M', O)}."""
@@ -80,10 +87,11 @@ def oracle_step(W, G, M, hp, which=None):
             out[k] = oracle.muon_slice(w, g, mm, hp["lr"], hp["beta"], hp["wd"], hp["nesterov"],
                                        T=hp["ns_steps"],
                                        coeffs=hp.get("coeffs", oracle.DEFAULT_COEFFS),
-                                       threads=threads)
+                                       scale=update_scale(*w.shape, hp), threads=threads)
         return out
     wo, mo, oo, _ = oracle.muon_slices(ws, gs, ms, hp["lr"], hp["beta"], hp["wd"], hp["nesterov"],
                                        T=hp["ns_steps"], coeffs=hp.get("coeffs", oracle.DEFAULT_COEFFS),
+                                       scales=[update_scale(*w.shape, hp) for w in ws],
                                        threads=threads)
     return {k: (wo[i], mo[i], oo[i]) for i, k in enumerate(keys)}
 
@@ -121,7 +129,7 @@ def compare(key, gpu, ref, W0, G, M0, hp, mode, dtype, report=None):
         # (1) the update arithmetic on the GPU's own O: W' is the RNE rounding
         #     of W*(1 - lr*wd) - lr*s*O within one bf16 ulp (fp32 intermediates)
         M_, N_ = W0.shape
-        s = float(np.float32(np.sqrt(max(1.0, M_ / N_))))
+        s = update_scale(M_, N_, hp)
         own = W0 * (1 - hp["lr"] * hp["wd"]) - hp["lr"] * s * Og
         own_b = torch.from_numpy(own).to(torch.bfloat16).double().numpy()
         # fp32 intermediates (decay, lr*s, the product) round at 2^-24 of
@@ -149,7 +157,8 @@ def run_and_check(shapes, dtype, hp, mode="tc16", grad_std=1e-2, seed=0, which=N
     m = muon()
     W, Gs, M = make_inputs(shapes, dtype, grad_std=grad_std, seed=seed)
     G = Gs[0]
-    plan = m.Plan([(tuple(s), dtype) for s in shapes], mode=mode, skinny_max_m=skinny_max_m)
+    plan = m.Plan([(tuple(s), dtype) for s in shapes], mode=mode, skinny_max_m=skinny_max_m,
+                  scale_mode=hp.get("scale_mode", "sqrt_ratio"))
     Wd = [w.cuda() for w in W]; Gd = [g.cuda() for g in G]; Md = [x.cuda() for x in M]
     O = gpu_step(plan, Wd, Gd, Md, hp)
     ref = oracle_step(W, G, M, hp, which)
@@ -167,14 +176,15 @@ def compare_folded(key, Wf, W0, G, M0, Og, ref, hp, dtype):
     On the fused skinny kernel that step folds the update factor -lr*s into
     the 16-bit left operand of its last product: it computes
     sum_k RNE16(-lr*s*Q~_ik) V_kj instead of -lr*s * sum_k RNE16(Q~_ik) V_kj,
-    with Q~ = Q/(||V|| + eps) and O = Q X0.  The two left operands differ by
-    at most 2^-8 relative per entry (one extra rounding of each, 2^-9 apiece;
-    bf16 has 8 significant bits), so the update term differs from the one of
-    the step that writes O (Og, same kernel, same V and fp32 Q bits) by at
-    most lr*s*2^-8*(|Q| |X0|)_ij.  Q is recovered from the oracle in fp64 as
+    with Q~ = Q/(||V|| + eps) and O = Q X0.  bf16 keeps 8 significant bits,
+    so one round-to-nearest moves a value by at most 2^-8 of itself; the two
+    left operands are rounded separately, so they differ by at most 2^-7
+    relative per entry, and the update term differs from the one of the step
+    that writes O (Og, same kernel, same V and fp32 Q bits) by at most
+    lr*s*2^-7*(|Q| |X0|)_ij.  Q is recovered from the oracle in fp64 as
     the m x m matrix with O = Q X0 (X0 has full row rank).  The bound per
     parameter, against the round-to-nearest value of the oracle's W':
-      ulp + lr*s*|Og - O_oracle| + 1.05 * lr*s*2^-8*(|Q| |X0|) + 4*2^-24*terms
+      ulp + lr*s*|Og - O_oracle| + 1.05 * lr*s*2^-7*(|Q| |X0|) + 4*2^-24*terms
     (the 5% covers the fp32 Q of the kernel against the fp64 one).  On the
     dense path the step without O is the same arithmetic as the one with O,
     so there the last two terms of the bound are not needed (the tests check
@@ -186,7 +196,7 @@ def compare_folded(key, Wf, W0, G, M0, Og, ref, hp, dtype):
     Og = np.asarray(Og.double().cpu().numpy(), np.float64)
     Wr, _, Or = ref
     M_, N_ = W0.shape
-    s = float(np.float32(np.sqrt(max(1.0, M_ / N_))))
+    s = update_scale(M_, N_, hp)
     lrs = hp["lr"] * s
     Mp = hp["beta"] * M0 + G
     V = G + hp["beta"] * Mp if hp["nesterov"] else Mp
@@ -205,8 +215,14 @@ def compare_folded(key, Wf, W0, G, M0, Og, ref, hp, dtype):
         Wr_r = Wr.astype(np.float32).astype(np.float64)
         ulp = np.maximum(np.spacing(np.abs(Wr_r).astype(np.float32)),
                          np.spacing(np.abs(Wf).astype(np.float32))).astype(np.float64)
-    bound = (ulp + lrs * np.abs(Og - Or) * 1.001 + 1.05 * lrs * 2.0 ** -8 * qx
-             + 4 * 2.0 ** -24 * terms)
-    bad = np.abs(Wf - Wr_r) > bound
-    assert not bad.any(), "slice %s: %d params of the step without O beyond the bound" % (
-        key, int(bad.sum()))
+    fold = 1.05 * lrs * 2.0 ** -7 * qx
+    bound = ulp + lrs * np.abs(Og - Or) * 1.001 + fold + 4 * 2.0 ** -24 * terms
+    diff = np.abs(Wf - Wr_r)
+    bad = diff > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(diff - bound), diff.shape)
+        raise AssertionError(
+            "slice %s: %d params of the step without O beyond the bound; worst at %s: "
+            "|W' - W'_oracle| %.3g, bound %.3g (ulp %.3g, O term %.3g, fold term %.3g)" % (
+                key, int(bad.sum()), i, diff[i], bound[i], ulp[i],
+                lrs * abs(Og[i] - Or[i]), fold[i]))

@@ -50,7 +50,7 @@ def _compare_plan(muon, shapes, dtypes_t, **kw):
     import torch
     plan = muon.Plan([(s, d) for s, d in zip(shapes, dtypes_t)], **kw)
     dts = ["bf16" if d == torch.bfloat16 else "f32" for d in dtypes_t]
-    sg, si, groups = oracle.plan(shapes, dts)
+    sg, si, groups = oracle.plan(shapes, dts, scale_mode=kw.get("scale_mode", "sqrt_ratio"))
     got = plan.groups()
     assert len(got) == len(groups)
     for a, b in zip(got, groups):
@@ -82,6 +82,54 @@ def test_plan_matches_oracle_random(muon):
             dts.append(torch.bfloat16 if rng.random() < 0.7 else torch.float32)
         _compare_plan(muon, shapes, dts)
         _compare_plan(muon, shapes, dts, mode="fp32")
+        _compare_plan(muon, shapes, dts, scale_mode="rms_match")
+
+
+def test_plan_log_lines(muon):
+    # MUON_LOG=1: muon_plan prints one line per group to stderr
+    import subprocess
+    import sys
+    code = ("import torch, newton_schulz_05_gb300 as m; "
+            "m.Plan([((24, 10240), torch.bfloat16), ((2, 1408, 2048), torch.bfloat16), "
+            "((2048, 1408), torch.bfloat16)])")
+    env = dict(os.environ, MUON_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    lines = [x for x in r.stderr.splitlines() if x.startswith("muon_plan:")]
+    assert lines[0].startswith("muon_plan: 3 parameters, 4 slices, 3 groups, workspace ")
+    assert "group 0 [24,10240] bf16 slices=1 m=24 n=10240 tr=0 scale=1 kernel=skinny cluster=2" \
+        in lines[1]
+    assert "group 1 [1408,2048] bf16 slices=2 m=1408 n=2048 tr=0" in lines[2] and \
+        "kernel=dense chunk=2" in lines[2]
+    assert "group 2 [2048,1408] bf16 slices=1 m=1408 n=2048 tr=1 scale=1.20604539" in lines[3]
+    env.pop("MUON_LOG")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert "muon_plan:" not in r.stderr
+
+
+def test_fault_switches_return_status_codes(muon, monkeypatch):
+    # MUON_FAULT=alloc: the plan fails as if host memory ran out; =launch:
+    # the step reports a failed launch after validating its arguments
+    import torch
+    monkeypatch.setenv("MUON_FAULT", "alloc")
+    with pytest.raises(muon.MuonError) as e:
+        muon.Plan([((24, 1000), torch.bfloat16)])
+    assert e.value.status == -8
+    monkeypatch.setenv("MUON_FAULT", "launch")
+    plan = muon.Plan([((24, 1000), torch.bfloat16)])
+    L = muon.load()
+    P = ctypes.c_void_p * 1
+    fake = P(ctypes.c_void_p(0x10000))
+    c = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    rc = L.muon_step(plan.handle, fake, fake, fake, 0.02, 0.95, 0.1, 1, 5, c,
+                     ctypes.c_void_p(0x100000), plan.workspace_bytes, None)
+    assert rc == -5
+    rc = L.muon_step(plan.handle, fake, fake, fake, float("nan"), 0.95, 0.1, 1, 5, c,
+                     ctypes.c_void_p(0x100000), plan.workspace_bytes, None)
+    assert rc == -1   # argument checks still come first
+    monkeypatch.delenv("MUON_FAULT")
 
 
 @pytest.mark.parametrize("name", ["fp32_24x1024", "skinny_74x24x10240", "stacks_experts",

@@ -41,6 +41,10 @@ MUTANTS = {
                            "group_N[k] == N"),
     "plan_scale_inverted": ("double ratio = (double)M / (double)N;",
                             "double ratio = (double)N / (double)M;"),
+    "plan_rms_scale_uses_min_dim": ("(float)(0.2 * std::sqrt((double)(M > N ? M : N)));",
+                                    "(float)(0.2 * std::sqrt((double)(M < N ? M : N)));"),
+    "plan_rms_scale_drops_factor": ("(float)(0.2 * std::sqrt((double)(M > N ? M : N)));",
+                                    "(float)(std::sqrt((double)(M > N ? M : N)));"),
     "finite_check_misses_nan": ("if (!std::isfinite(G[i])) return 0;",
                                 "if (std::isinf(G[i])) return 0;"),
     "unscale_divides": ("out[i] = G[i] * inv_scale;", "out[i] = G[i] / inv_scale;"),

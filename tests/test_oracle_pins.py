@@ -269,6 +269,28 @@ def test_plan_random_shape_lists():
         _check_plan(shapes, dtypes)
 
 
+def test_plan_rms_match_scale_gives_update_rms_of_one_fifth():
+    # scale_mode "rms_match": s O has RMS 0.2 when O has unit singular values
+    # (O O^T = I for M <= N): RMS(O) = sqrt(min(M,N) / (M N)) = 1/sqrt(max(M,N))
+    rng = np.random.default_rng(31)
+    shapes = [(24, 10240), (64, 64), (300, 70), (70, 300), (4096, 11008), (11008, 4096)]
+    _, _, groups = oracle.plan(shapes, ["bf16"] * len(shapes), scale_mode="rms_match")
+    assert [(g["M"], g["N"]) for g in groups] == shapes
+    for (M, N), g in zip(shapes, groups):
+        k = min(M, N)
+        if M * N <= 300 * 300:
+            Q, _ = np.linalg.qr(rng.standard_normal((max(M, N), k)))
+            O = Q.T if M <= N else Q            # unit singular values, shape (M, N)
+            rms = np.sqrt(np.mean((g["scale"] * O) ** 2))
+        else:
+            rms = g["scale"] * np.sqrt(k / (M * N))
+        assert abs(rms - 0.2) < 1e-6, (M, N, rms)
+    # symmetric in M and N, unlike sqrt(max(1, M/N))
+    assert groups[2]["scale"] == groups[3]["scale"] and groups[4]["scale"] == groups[5]["scale"]
+    # tabulated: 0.2 sqrt(10240) = 20.238577..., 0.2 sqrt(64) = 1.6
+    assert abs(groups[0]["scale"] - 20.2385770) < 1e-5 and groups[1]["scale"] == np.float32(1.6)
+
+
 def test_plan_rejects_bad_shapes():
     for bad in [[(5,)], [(2, 3, 4, 5)], [(0, 4)], [(3, 0, 2)]]:
         with pytest.raises(ValueError):

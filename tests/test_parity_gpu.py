@@ -77,6 +77,27 @@ def test_plain_momentum_and_cubic_coefficients(shape):
     run_and_check([shape], torch.float32, dict(HP, coeffs=(1.5, -0.5, 0.0), ns_steps=10))
 
 
+@pytest.mark.parametrize("shape", [(24, 1000), (24, 10240), (200, 300), (300, 200), (1000, 70)],
+                         ids=str)
+def test_rms_match_update_scale(shape):
+    # s = 0.2 sqrt(max(M, N)) in place of sqrt(max(1, M/N)), both calls
+    hp = dict(HP, scale_mode="rms_match")
+    run_and_check([shape], torch.bfloat16, hp)
+    m = muon()
+    W, Gs, M = make_inputs([shape], torch.bfloat16)
+    plan = m.Plan([(shape, torch.bfloat16)], scale_mode="rms_match")
+    assert abs(plan.groups()[0]["scale"] - 0.2 * max(shape) ** 0.5) < 1e-5
+    Wd, Md = [W[0].cuda()], [M[0].cuda()]
+    Wb, Mb = [W[0].cuda()], [M[0].cuda()]
+    O = gpu_step(plan, Wb, [Gs[0][0].cuda()], Mb, hp)
+    gpu_step(plan, Wd, [Gs[0][0].cuda()], Md, hp, ortho=False)
+    ref = oracle_step(W, Gs[0], M, hp)
+    assert torch.equal(Md[0], Mb[0])
+    from helpers import compare_folded
+    compare_folded((0, 0), Wd[0].cpu(), W[0], Gs[0][0], M[0], O[0].cpu(), ref[(0, 0)], hp,
+                   torch.bfloat16)
+
+
 @pytest.mark.parametrize("shape", [(24, 1000), (200, 300), (300, 200)], ids=str)
 def test_zero_gradient_is_pure_decay(shape):
     m = muon()
