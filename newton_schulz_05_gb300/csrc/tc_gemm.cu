@@ -25,6 +25,8 @@
 #include <cudaTypedefs.h>
 
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -297,6 +299,77 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& b, in
   I = 0; J = 0;  // unreachable for valid t
 }
 
+// Epilogue of one accumulator tile for the calling warp (all lanes): its
+// 32 rows row0 + lane of 128-row block I, the BN columns from J * BN, read
+// from tensor memory at `tacc`; scaled rows (plus the diagonal term) go to
+// D (and D2) through the warp's staging slot and TMA tensor stores, a
+// symmetric product's block above the diagonal also to its mirror, or, with
+// a fused update, into the parameters.  ck counts the chunks staged so far.
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorMap* tmD,
+                                              const CUtensorMap* tmD2, uint32_t tacc,
+                                              unsigned char* epi_slot, int b, int I, int row0,
+                                              int J, uint32_t& ck) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t slot = smem_u32(epi_slot);
+  // staging bytes of one 32-column chunk; the slot holds EPI_BYTES / that
+  // many chunks in flight
+  const int cbytes = (p.d_f32 ? 4096 : 2048) * (p.sym ? 2 : 1) * (p.has_d2 ? 2 : 1);
+  const int nbuf = EPI_BYTES / cbytes;
+  const int row = row0 + lane;
+  #pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int col0 = J * BN + c * 32;
+    if (col0 >= p.N) continue;
+    const int cblk = col0 / 128;
+    if (p.sym && cblk < I) continue;  // lower block: written as a mirror by its owner
+    const bool mirror = p.sym && cblk > I;
+    float v[32], v2[32];
+    tm_ld32(tacc + c * 32, v);
+    const bool dg = row >= col0 && row < col0 + 32;   // the diagonal crosses this row
+    #pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float d = (dg && col0 + j == row) ? 1.f : 0.f;
+      v2[j] = fmaf(p.alpha2, v[j], d * p.diag2);
+      v[j] = fmaf(p.alpha, v[j], d * p.diag);
+    }
+    if (p.fuse) {
+      float* tile = reinterpret_cast<float*>(epi_slot);
+      if (p.w_f32) fused_update<float>(p, static_cast<float*>(p.W[b]), row0, col0, v, tile);
+      else fused_update<__nv_bfloat16>(p, static_cast<__nv_bfloat16*>(p.W[b]), row0, col0, v, tile);
+      continue;
+    }
+    // the staging buffer of this chunk is free once the stores issued from
+    // it nbuf chunks ago have read it
+    if (lane == 0) bulk_wait_read(nbuf - 1);
+    __syncwarp();
+    const uint32_t buf = slot + (ck % nbuf) * cbytes;
+    if (p.d_f32) {
+      stage_row_f(buf, lane, v);
+    } else {
+      stage_row_h(buf, lane, v);
+      if (mirror) stage_col_h(buf + 2048, lane, v);
+      if (p.has_d2) {
+        const uint32_t b2 = buf + (p.sym ? 4096 : 2048);
+        stage_row_h(b2, lane, v2);
+        if (mirror) stage_col_h(b2 + 2048, lane, v2);
+      }
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tmD, buf, col0, row0, b);
+      if (mirror) tma_store_3d(tmD, buf + 2048, row0, col0, b);
+      if (p.has_d2) {
+        const uint32_t b2 = buf + (p.sym ? 4096 : 2048);
+        tma_store_3d(tmD2, b2, col0, row0, b);
+        if (mirror) tma_store_3d(tmD2, b2 + 2048, row0, col0, b);
+      }
+      bulk_commit();
+    }
+    ++ck;
+  }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
@@ -422,11 +495,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else {
     // epilogue warps 2..5: TMEM lane quarter q = warp % 4, 32 rows each
     const int q = warp & 3;
-    const uint32_t slot = smem_u32(epi + q * EPI_BYTES);
-    // staging bytes of one 32-column chunk; the slot holds EPI_BYTES / that
-    // many chunks in flight
-    const int cbytes = (p.d_f32 ? 4096 : 2048) * (p.sym ? 2 : 1) * (p.has_d2 ? 2 : 1);
-    const int nbuf = EPI_BYTES / cbytes;
     uint32_t ck = 0, tl = 0;
     for (int t = blockIdx.x; t < p.total_tiles && !*abort_flag; t += gridDim.x, ++tl) {
       int b, I, J;
@@ -434,60 +502,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
       if (!mbar_wait(&tfull[acc], aph, p.wait_limit)) { fail(); break; }
       tc_fence_after();
-      const int row0 = I * BM + q * 32;
-      const int row = row0 + lane;
-      #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = J * BN + c * 32;
-        if (col0 >= p.N) continue;
-        const int cblk = col0 / 128;
-        if (p.sym && cblk < I) continue;  // lower block: written as a mirror by its owner
-        const bool mirror = p.sym && cblk > I;
-        float v[32], v2[32];
-        tm_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, v);
-        const bool dg = row >= col0 && row < col0 + 32;   // the diagonal crosses this row
-        #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float d = (dg && col0 + j == row) ? 1.f : 0.f;
-          v2[j] = fmaf(p.alpha2, v[j], d * p.diag2);
-          v[j] = fmaf(p.alpha, v[j], d * p.diag);
-        }
-        if (p.fuse) {
-          float* tile = reinterpret_cast<float*>(epi + q * EPI_BYTES);
-          if (p.w_f32) fused_update<float>(p, static_cast<float*>(p.W[b]), row0, col0, v, tile);
-          else fused_update<__nv_bfloat16>(p, static_cast<__nv_bfloat16*>(p.W[b]), row0, col0, v, tile);
-          continue;
-        }
-        // the staging buffer of this chunk is free once the stores issued from
-        // it nbuf chunks ago have read it
-        if (lane == 0) bulk_wait_read(nbuf - 1);
-        __syncwarp();
-        const uint32_t buf = slot + (ck % nbuf) * cbytes;
-        if (p.d_f32) {
-          stage_row_f(buf, lane, v);
-        } else {
-          stage_row_h(buf, lane, v);
-          if (mirror) stage_col_h(buf + 2048, lane, v);
-          if (p.has_d2) {
-            const uint32_t b2 = buf + (p.sym ? 4096 : 2048);
-            stage_row_h(b2, lane, v2);
-            if (mirror) stage_col_h(b2 + 2048, lane, v2);
-          }
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&tmD, buf, col0, row0, b);
-          if (mirror) tma_store_3d(&tmD, buf + 2048, row0, col0, b);
-          if (p.has_d2) {
-            const uint32_t b2 = buf + (p.sym ? 4096 : 2048);
-            tma_store_3d(&tmD2, b2, col0, row0, b);
-            if (mirror) tma_store_3d(&tmD2, b2 + 2048, row0, col0, b);
-          }
-          bulk_commit();
-        }
-        ++ck;
-      }
+      epilogue_tile(p, &tmD, &tmD2, tmem + ((uint32_t)(q * 32) << 16) + acc * BN, epi + q * EPI_BYTES,
+                    b, I, I * BM + q * 32, J, ck);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -501,6 +517,265 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Pair kernel: the same products on CTA pairs (thread-block clusters of two
+// CTAs on two SMs), with 2-SM MMAs (tcgen05.mma.cta_group::2, M = 256):
+// a pair computes a 256 x 256 output tile; CTA r holds rows
+// [256 I2 + 128 r, +128) of A and the B rows (K-major) or columns (N-major)
+// [256 J + 128 r, +128) in its own shared memory, and its 128 x 256 fp32
+// accumulator in its own tensor memory.  Per CTA and k-block a stage is
+// 32 KB instead of 48 KB, so six stages are in flight instead of four and a
+// CTA moves two thirds of the operand bytes per MMA flop.
+//
+// Roles per CTA (6 warps): warp 0 loads its operand halves into its own
+// stages (counted on its own `loaded` barrier, so that it can always wait
+// for its own copies); in CTA 1, warp 1 relays each landed stage to CTA 0
+// (remote arrive on CTA 0's `ready` barrier); in CTA 0, warp 1 issues the
+// pair's MMAs once both halves of a stage are in and releases stages and
+// accumulators to both CTAs by multicast commits; warps 2-5 of both CTAs run
+// the epilogue of their 128 rows and report to CTA 0's `tempty` barrier.
+constexpr int PSTAGES = 6;
+constexpr int B_HALF = 128 * BK * 2;               // 16 KB: this CTA's half of B
+constexpr int PSTAGE_BYTES = A_BYTES + B_HALF;     // 32 KB
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
+                   : "memory");
+}
+// bounded wait at cluster scope (the phase may be completed from the peer CTA)
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity,
+                                             uint32_t limit = kWaitLimit) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void mma2_f16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// arrive on the barrier at this offset in both CTAs of the pair once every
+// MMA issued so far by this thread has completed
+__device__ __forceinline__ void mma2_commit_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;\n" ::"r"(smem_u32(bar)), "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_commit_local(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// pair tile index -> (batch, 256-row tile I2, 256-column tile J); symmetric
+// outputs enumerate the tiles with J >= I2
+__device__ __forceinline__ void pair_tile_coords(const TcParams& p, int t, int& b, int& I2, int& J) {
+  b = t / p.tiles_per_batch;
+  int r = t % p.tiles_per_batch;
+  if (!p.sym) {
+    I2 = r / p.tiles_n;
+    J = r % p.tiles_n;
+    return;
+  }
+  for (I2 = 0; I2 < p.tiles_n; ++I2) {
+    const int cnt = p.tiles_n - I2;
+    if (r < cnt) { J = I2 + r; return; }
+    r -= cnt;
+  }
+  I2 = 0; J = 0;  // unreachable for valid t
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
+                    const __grid_constant__ TcParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* epi = smem + PSTAGES * PSTAGE_BYTES;    // 4 x EPI_BYTES staging
+  uint64_t* loaded = reinterpret_cast<uint64_t*>(epi + 4 * EPI_BYTES);  // own stage landed
+  uint64_t* ready = loaded + PSTAGES;    // CTA 0: the peer's stage landed (relayed)
+  uint64_t* empty = ready + PSTAGES;     // stage free (multicast commit)
+  uint64_t* tfull = empty + PSTAGES;     // accumulator ready (multicast commit)
+  uint64_t* tempty = tfull + 2;          // CTA 0: accumulator drained by all 8 epilogue warps
+  uint64_t* mdrain = tempty + 2;         // CTA 0: every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdrain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      mbar_init(&loaded[s], 1); mbar_init(&ready[s], 1); mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 8); }
+    mbar_init(mdrain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  if (warp == 1) {
+    // one warp of each CTA of the pair allocates, collectively
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
+                     smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // barriers of both CTAs initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int kblocks = p.K / BK;
+  pdl_wait();
+  const bool skipped = (p.skip && *p.skip) || *static_cast<volatile int*>(p.err) != 0;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicExch(p.err, kDevErrTimeout);
+  };
+
+  if (skipped) {
+    // no role runs; only the teardown below
+  } else if (warp == 0) {
+    if (lane == 0) {
+      // producer: this CTA's halves of every stage, on its own barrier
+      uint32_t it = 0;
+      for (int t = pair; t < p.total_tiles && !*abort_flag; t += npairs) {
+        int b, I2, J;
+        pair_tile_coords(p, t, b, I2, J);
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % PSTAGES;
+          const uint32_t ph = (it / PSTAGES) & 1;
+          if (!mbar_wait_cl(&empty[s], ph ^ 1, p.wait_limit)) { fail(); break; }
+          unsigned char* sa = smem + s * PSTAGE_BYTES;
+          unsigned char* sb = sa + A_BYTES;
+          mbar_expect_tx(&loaded[s], PSTAGE_BYTES);
+          tma_load_3d(sa, &tmA, &loaded[s], kb * BK, I2 * 256 + (int)rank * 128, b);
+          if (!p.b_mn) {
+            tma_load_3d(sb, &tmB, &loaded[s], kb * BK, J * 256 + (int)rank * 128, b);
+          } else {
+            #pragma unroll
+            for (int q = 0; q < 2; ++q)
+              tma_load_3d(sb + q * (64 * BK * 2), &tmB, &loaded[s], J * 256 + (int)rank * 128 + q * 64,
+                          kb * BK, b);
+          }
+        }
+      }
+      // every issued load lands before the CTA may leave
+      const uint32_t last = it;
+      for (uint32_t k = (last > PSTAGES ? last - PSTAGES : 0); k < last; ++k)
+        if (!mbar_wait(&loaded[k % PSTAGES], (k / PSTAGES) & 1)) { fail(); break; }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 1) {
+      // relay: each stage of this CTA that has landed is reported to CTA 0
+      uint32_t it = 0;
+      for (int t = pair; t < p.total_tiles && !*abort_flag; t += npairs) {
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % PSTAGES;
+          const uint32_t ph = (it / PSTAGES) & 1;
+          if (!mbar_wait(&loaded[s], ph, p.wait_limit)) { fail(); ok = false; break; }
+          mbar_arrive_remote(mapa(smem_u32(&ready[s]), 0));
+        }
+        if (!ok) break;
+      }
+    } else if (lane == 0) {
+      // CTA 0: the pair's MMAs (M = 256, N = 256, K = 16)
+      uint32_t it = 0, tl = 0;
+      for (int t = pair; t < p.total_tiles && !*abort_flag; t += npairs, ++tl) {
+        const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
+        if (!mbar_wait_cl(&tempty[acc], aph ^ 1, p.wait_limit)) { fail(); break; }
+        tc_fence_after();
+        const uint32_t dt = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % PSTAGES;
+          const uint32_t ph = (it / PSTAGES) & 1;
+          if (!mbar_wait(&loaded[s], ph, p.wait_limit) ||
+              !mbar_wait_cl(&ready[s], ph, p.wait_limit)) {
+            fail(); ok = false; break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * PSTAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          #pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc(sa + k * 32, 16, 1024);
+            const uint64_t bd = p.b_mn ? sdesc(sb + k * 2048, 64 * BK * 2, 1024)
+                                       : sdesc(sb + k * 32, 16, 1024);
+            mma2_f16(dt, ad, bd, p.idesc, (kb | k) != 0);
+          }
+          mma2_commit_both(&empty[s]);
+        }
+        if (!ok) break;
+        mma2_commit_both(&tfull[acc]);
+      }
+      // every MMA issued above completes before either CTA releases its
+      // shared or tensor memory
+      if (it > 0) {
+        mma2_commit_local(mdrain);
+        if (!mbar_wait(mdrain, 0)) fail();
+      }
+    }
+  } else {
+    // epilogue warps 2..5 of both CTAs: TMEM lane quarter q, 32 rows each
+    const int q = warp & 3;
+    uint32_t ck = 0, tl = 0;
+    for (int t = pair; t < p.total_tiles && !*abort_flag; t += npairs, ++tl) {
+      int b, I2, J;
+      pair_tile_coords(p, t, b, I2, J);
+      const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
+      if (!mbar_wait_cl(&tfull[acc], aph, p.wait_limit)) { fail(); break; }
+      tc_fence_after();
+      const int I = 2 * I2 + (int)rank;    // 128-row block of this CTA
+      if (I * BM < p.M)                    // past M: rows of zeros, nothing to store
+        epilogue_tile(p, &tmD, &tmD2, tmem + ((uint32_t)(q * 32) << 16) + acc * BN,
+                      epi + q * EPI_BYTES, b, I, I * BM + q * 32, J, ck);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa(smem_u32(&tempty[acc]), 0));
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // the peer's MMAs and remote arrives are done with this CTA
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -561,9 +836,46 @@ uint32_t tc_idesc_f16(int m, int n, int b_mn) {
 
 size_t tc_gemm_smem_bytes() { return STAGES * STAGE_BYTES + 4 * EPI_BYTES + 1024 + 256; }
 
+// the pair kernel for products with at least one 256-row tile, unless
+// MUON_GEMM=single selects the one-CTA kernel (for comparisons)
+static bool use_pair_kernel(const TcGemm& g) {
+  if (g.M < 256) return false;
+  const char* e = std::getenv("MUON_GEMM");
+  return !(e && std::strcmp(e, "single") == 0);
+}
+
+size_t tc_gemm_pair_smem_bytes() {
+  return PSTAGES * PSTAGE_BYTES + 4 * EPI_BYTES + 1024 + 256;
+}
+
+// pairs of CTAs that can be resident at once (one CTA per SM), per device
+static int max_pairs(size_t smem) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 76);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0)
+    n = num_sms() / 2;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
 cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
   if (g.M % BM || g.N % 128 || g.K % BK || g.batch < 1 || (g.sym && g.M != g.N))
     return cudaErrorInvalidValue;
+  const bool pair = use_pair_kernel(g);
   CUtensorMap ta, tb;
   if (!make_map(&ta, g.A, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.batch, (uint64_t)g.K * 2,
                 g.stride, BK, BM))
@@ -572,7 +884,7 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
       ? make_map(&tb, g.B, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)g.batch, (uint64_t)g.N * 2, g.stride,
                  64, BK)
       : make_map(&tb, g.B, (uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.batch, (uint64_t)g.K * 2, g.stride,
-                 BK, BN);
+                 BK, pair ? 128 : BN);
   if (!ok_b) return cudaErrorInvalidValue;
   if (g.d_f32 && (g.sym || g.D2)) return cudaErrorInvalidValue;   // mirrors and D2 are fp16
   CUtensorMap td, td2;
@@ -589,13 +901,18 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
   }
   TcParams p;
   p.M = (int)g.M; p.N = (int)g.N; p.K = (int)g.K;
-  p.tiles_m = (int)(g.M / BM);
   p.tiles_n = (int)((g.N + BN - 1) / BN);
-  if (g.sym) {
+  if (pair) {
+    // 256 x 256 tiles; symmetric: the tiles with J >= I2
+    p.tiles_m = (int)((g.M + 255) / 256);
+    p.tiles_per_batch = g.sym ? p.tiles_n * (p.tiles_n + 1) / 2 : p.tiles_m * p.tiles_n;
+  } else if (g.sym) {
+    p.tiles_m = (int)(g.M / BM);
     int cnt = 0;
     for (int I = 0; I < p.tiles_m; ++I) cnt += p.tiles_n - I / 2;
     p.tiles_per_batch = cnt;
   } else {
+    p.tiles_m = (int)(g.M / BM);
     p.tiles_per_batch = p.tiles_m * p.tiles_n;
   }
   p.total_tiles = p.tiles_per_batch * g.batch;
@@ -620,11 +937,36 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
   p.alpha = g.alpha; p.diag = g.diag;
   p.alpha2 = g.alpha2; p.diag2 = g.diag2;
   p.sym = g.sym; p.b_mn = g.b_mn;
-  p.idesc = tc_idesc_f16(BM, BN, g.b_mn);
+  p.idesc = pair ? tc_idesc_f16(256, BN, g.b_mn) : tc_idesc_f16(BM, BN, g.b_mn);
   p.idesc128 = tc_idesc_f16(BM, 128, g.b_mn);
   p.err = g.err;
   p.skip = g.skip;
   p.wait_limit = g.wait_limit;
+  if (pair) {
+    const size_t smem = tc_gemm_pair_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int np = max_pairs(smem);
+    const int pairs = p.total_tiles < np ? p.total_tiles : np;
+    // thread-block clusters of two CTAs, launched as a dependent of the
+    // previous kernel of the step
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, ta, tb, td, td2, p);
+  }
   const size_t smem = tc_gemm_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
