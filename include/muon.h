@@ -275,6 +275,36 @@ MUON_API muon_status muon_step_static(const muon_plan_t* plan, void* const* para
  */
 MUON_API muon_status muon_static_error(void* stream, int clear, int* code);
 
+/* kernel classes of muon_step_timed */
+enum {
+  MUON_KC_SKINNY = 0,  /* fused on-chip kernel of the skinny groups              */
+  MUON_KC_FRONT = 1,   /* dense path: momentum, V, partial sums of V^2           */
+  MUON_KC_NORM = 2,    /* dense path: 1/(||V|| + eps) and the 16-bit X0          */
+  MUON_KC_GEMM = 3,    /* dense path: the tcgen05 (or fp32) Newton-Schulz products */
+  MUON_KC_UPDATE = 4,  /* dense path: separate update kernel (O requested)       */
+  MUON_KC_CHECK = 5,   /* loss-scaled step: non-finite check of the gradients    */
+  MUON_KC_COUNT = 6
+};
+typedef struct {
+  float ms[MUON_KC_COUNT];   /* device time summed over the launches of a class  */
+  int launches[MUON_KC_COUNT];
+} muon_kernel_times;
+
+/*
+ * muon_step with a CUDA event recorded on `stream` before every kernel
+ * launch and after the last one; synchronises `stream` and writes the device
+ * time of each kernel class into *times (host).  An event between two
+ * launches keeps a kernel from overlapping its predecessor's tail, so the
+ * classes can sum to slightly more than a muon_step of the same plan takes.
+ * For measurement: it creates and destroys its events (host-side driver
+ * objects, no device memory).  Other arguments are those of muon_step.
+ */
+MUON_API muon_status muon_step_timed(const muon_plan_t* plan, void* const* params,
+                                     const void* const* grads, float* const* momentum,
+                                     float lr, float beta, float wd, int nesterov, int ns_steps,
+                                     const float* coeffs, void* workspace, size_t ws_bytes,
+                                     void* stream, muon_kernel_times* times);
+
 /* Kernel launches muon_step makes for this plan and ns_steps, for a step
  * without O outputs (for accounting; no device call). */
 MUON_API muon_status muon_plan_launches(const muon_plan_t* plan, int ns_steps, int* out);

@@ -57,11 +57,20 @@ class _GroupInfo(ctypes.Structure):
                 ("cluster", ctypes.c_int), ("chunk", ctypes.c_int)]
 
 
+KERNEL_CLASSES = ("skinny", "front", "norm", "gemm", "update", "check")   # MUON_KC_*
+
+
+class _KernelTimes(ctypes.Structure):
+    _fields_ = [("ms", ctypes.c_float * len(KERNEL_CLASSES)),
+                ("launches", ctypes.c_int * len(KERNEL_CLASSES))]
+
+
 EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
            "muon_plan_num_groups", "muon_plan_num_slices", "muon_plan_group",
            "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
            "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static",
-           "muon_step_amp", "muon_adamw_step", "muon_plan_partition", "muon_static_error"]
+           "muon_step_amp", "muon_adamw_step", "muon_plan_partition", "muon_static_error",
+           "muon_step_timed"]
 
 STATIC_WORKSPACE_BYTES = 32 << 20   # MUON_STATIC_WORKSPACE_BYTES in include/muon.h
 
@@ -98,6 +107,7 @@ def load(path: str = LIB_PATH):
                  ctypes.c_int, ctypes.POINTER(ctypes.c_float), vp, sz, vp]
     L.muon_step.argtypes = step_args
     L.muon_step_ortho.argtypes = step_args + [PP]
+    L.muon_step_timed.argtypes = step_args + [ctypes.POINTER(_KernelTimes)]
     L.muon_step_static.argtypes = step_args[:10] + [vp]
     L.muon_step_amp.argtypes = step_args[:10] + [ctypes.c_float, vp, vp, sz, vp]
     L.muon_adamw_step.argtypes = [ctypes.c_int, PP, PP, PP, PP, ctypes.POINTER(ctypes.c_int64),
@@ -117,7 +127,7 @@ def load(path: str = LIB_PATH):
                "muon_plan_num_slices", "muon_plan_group", "muon_plan_slice", "muon_step",
                "muon_step_ortho", "muon_workspace_error", "muon_plan_launches",
                "muon_step_static", "muon_step_amp", "muon_adamw_step", "muon_plan_partition",
-               "muon_static_error"):
+               "muon_static_error", "muon_step_timed"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -412,6 +422,16 @@ class PreparedStep:
 
     def __call__(self) -> None:
         _check(self._fn(*self._args), "muon_step")
+
+    def timed(self) -> dict:
+        """The same step through muon_step_timed (not with O outputs): a CUDA
+        event before every launch; synchronises the stream and returns
+        {kernel class: (device ms, launches)}."""
+        if len(self._args) != 13:
+            raise ValueError("timed steps do not write O")
+        t = _KernelTimes()
+        _check(load().muon_step_timed(*self._args, ctypes.byref(t)), "muon_step_timed")
+        return {k: (t.ms[i], t.launches[i]) for i, k in enumerate(KERNEL_CLASSES)}
 
 
 class Partition:

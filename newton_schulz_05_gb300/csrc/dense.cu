@@ -292,6 +292,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   cudaError_t le;
   {
     NvtxRange r("muon::front_kernel");
+    st.mark(MUON_KC_FRONT);
     if (g.dtype == MUON_BF16)
       le = launch_k(front_kernel<__nv_bfloat16>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m,
                     g.n, mp, np, (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip,
@@ -304,6 +305,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   if (le != cudaSuccess) return le;
   {
     NvtxRange r("muon::finalize_kernel");
+    st.mark(MUON_KC_NORM);
     le = launch_k(finalize_kernel, dim3(ns), dim3(kNT), 0, s, true, ws, sws, off.part, off.inv,
                   nblk, st.eps, (const int*)err_word);
   }
@@ -313,6 +315,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   if (nb > 1184) nb = 1184;
   {
     NvtxRange r("muon::normalize_kernel");
+    st.mark(MUON_KC_NORM);
     le = launch_k(normalize_kernel<IT>, dim3(nb, ns), dim3(kNT), 0, s, true, ws, sws, off.V,
                   off.X0, off.inv, cnt, st.T == 0 ? 1 : 0, (const int*)err_word);
   }
@@ -344,6 +347,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
       cudaError_t e;
       {
         NvtxRange r("muon::tc_gemm gram");
+        st.mark(MUON_KC_GEMM);
         e = tc_gemm(g1, s);
       }
       if (e != cudaSuccess) return e;
@@ -356,6 +360,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
       g2.diag = st.a;
       {
         NvtxRange r("muon::tc_gemm poly");
+        st.mark(MUON_KC_GEMM);
         e = tc_gemm(g2, s);
       }
       if (e != cudaSuccess) return e;
@@ -375,6 +380,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
       }
       {
         NvtxRange r("muon::tc_gemm update");
+        st.mark(MUON_KC_GEMM);
         e = tc_gemm(g3, s);
       }
       if (e != cudaSuccess) return e;
@@ -390,18 +396,21 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
     gb.M = mp; gb.N = mp; gb.K = np;
     gb.A = ws + xin; gb.B = ws + xin; gb.C = nullptr; gb.D = ws + off.A;
     gb.alpha = 1.f; gb.beta = 0.f;
+    st.mark(MUON_KC_GEMM);
     cudaError_t e = gemm_nt<IT, IT>(gb, s);
     if (e != cudaSuccess) return e;
     // B = c*(A A) + b*A                 A symmetric: A A = A A^T
     gb.M = mp; gb.N = mp; gb.K = mp;
     gb.A = ws + off.A; gb.B = ws + off.A; gb.C = ws + off.A; gb.D = ws + off.B;
     gb.alpha = st.c; gb.beta = st.b;
+    st.mark(MUON_KC_GEMM);
     e = gemm_nt<IT, IT>(gb, s);
     if (e != cudaSuccess) return e;
     // X' = B X + a*X                    [m_pad, n_pad], K = m_pad, X is N-major
     gb.M = mp; gb.N = np; gb.K = mp;
     gb.A = ws + off.B; gb.B = ws + xin; gb.C = ws + xin;
     gb.alpha = 1.f; gb.beta = st.a;
+    st.mark(MUON_KC_GEMM);
     if (last) {
       gb.D = ws + off.V;
       e = gemm_nn<IT, float>(gb, s);
@@ -416,6 +425,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
                                    : (int)(((g.M + 31) / 32) * ((g.N + 31) / 32));
   if (fuse) return cudaSuccess;   // the last product updated the parameters
   NvtxRange r("muon::epilogue_kernel");
+  st.mark(MUON_KC_UPDATE);
   if (g.dtype == MUON_BF16)
     return launch_k(epilogue_kernel<__nv_bfloat16>, dim3(tiles, ns), dim3(kNT), 0, s, true, ptrs,
                     g.M, g.N, np, (int)g.tr, vec, decay, lrs, st.skip, (const int*)err_word, ws,

@@ -79,6 +79,24 @@ struct SlicePtrs {
   float* O[kMaxSlicesPerLaunch];     // null entries: O not requested
 };
 
+// Events recorded before every kernel launch of a step (muon_step_timed):
+// interval i, from event i to event i + 1, is the kernel of class cls[i].
+struct LaunchTimer {
+  cudaStream_t stream = nullptr;
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> cls;
+  cudaError_t err = cudaSuccess;
+  void mark(int c) {
+    cudaEvent_t e = nullptr;
+    if (err == cudaSuccess) err = cudaEventCreate(&e);
+    if (err == cudaSuccess) err = cudaEventRecord(e, stream);
+    if (e) { ev.push_back(e); cls.push_back(c); }
+  }
+  ~LaunchTimer() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+};
+
 struct StepArgs {
   float lr, beta, wd;
   int nesterov;
@@ -88,6 +106,10 @@ struct StepArgs {
   float gscale = 1.f;          // gradients are multiplied by this (1/loss scale)
   const int* skip = nullptr;   // device flag: when set, the step changes nothing
   uint32_t wait_limit = kWaitLimit;   // polls of a bounded wait on the main path
+  LaunchTimer* timer = nullptr;       // per-launch events (measurement only)
+  void mark(int kernel_class) const {
+    if (timer) timer->mark(kernel_class);
+  }
 };
 
 size_t dense_slice_ws(const Group& g, int mode);

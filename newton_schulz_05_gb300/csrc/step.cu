@@ -16,7 +16,7 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
                       float* const* momentum, float lr, float beta, float wd, int nesterov,
                       int ns_steps, const float* coeffs, void* workspace, size_t ws_bytes,
                       void* stream, float* const* ortho, float inv_scale = 1.f,
-                      int* found_inf = nullptr) {
+                      int* found_inf = nullptr, LaunchTimer* timer = nullptr) {
   if (!P) return MUON_ERR_INVALID_ARG;
   NvtxRange range(found_inf ? "muon_step_amp" : ortho ? "muon_step_ortho" : "muon_step");
   const int np = (int)P->shapes.size();
@@ -39,6 +39,7 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
   if (!std::isfinite(inv_scale)) return MUON_ERR_INVALID_ARG;
   st.gscale = inv_scale;
   st.skip = found_inf;
+  st.timer = timer;
   const int fault = fault_switch();
   if (fault == kFaultLaunch) return MUON_ERR_CUDA;
   if (fault == kFaultTimeout) st.wait_limit = 0;
@@ -68,6 +69,7 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
       for (int c0 = 0; c0 < g.count(); c0 += kMaxSlicesPerLaunch) {
         const int ns = g.count() - c0 < kMaxSlicesPerLaunch ? g.count() - c0 : kMaxSlicesPerLaunch;
         fill(g, c0, ns);
+        st.mark(MUON_KC_CHECK);
         if (launch_check_finite(g, ptrs, ns, found_inf, s) != cudaSuccess) return MUON_ERR_CUDA;
       }
   }
@@ -82,6 +84,7 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
       cudaError_t e;
       if (g.kernel == MUON_KERNEL_SKINNY) {
         NvtxRange r("muon::skinny_kernel");
+        st.mark(MUON_KC_SKINNY);
         e = launch_skinny(g, ptrs, ns, st, err_word, s);
       } else {
         e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body, err_word, s, !first);
@@ -122,6 +125,32 @@ muon_status muon_step_amp(const muon_plan_t* P, void* const* params, const void*
   if (!found_inf) return MUON_ERR_INVALID_ARG;
   return step_impl(P, params, grads, momentum, lr, beta, wd, nesterov, ns_steps, coeffs,
                    workspace, ws_bytes, stream, nullptr, inv_scale, found_inf);
+}
+
+muon_status muon_step_timed(const muon_plan_t* P, void* const* params, const void* const* grads,
+                            float* const* momentum, float lr, float beta, float wd, int nesterov,
+                            int ns_steps, const float* coeffs, void* workspace, size_t ws_bytes,
+                            void* stream, muon_kernel_times* times) {
+  if (!times) return MUON_ERR_INVALID_ARG;
+  LaunchTimer timer;
+  timer.stream = static_cast<cudaStream_t>(stream);
+  const muon_status st = step_impl(P, params, grads, momentum, lr, beta, wd, nesterov, ns_steps,
+                                   coeffs, workspace, ws_bytes, stream, nullptr, 1.f, nullptr,
+                                   &timer);
+  if (st != MUON_OK) return st;
+  timer.mark(-1);   // end of the last launch
+  if (timer.err != cudaSuccess) return MUON_ERR_CUDA;
+  if (cudaStreamSynchronize(timer.stream) != cudaSuccess) return MUON_ERR_CUDA;
+  for (int k = 0; k < MUON_KC_COUNT; ++k) { times->ms[k] = 0.f; times->launches[k] = 0; }
+  for (size_t i = 0; i + 1 < timer.ev.size(); ++i) {
+    const int c = timer.cls[i];
+    if (c < 0 || c >= MUON_KC_COUNT) continue;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, timer.ev[i], timer.ev[i + 1]) != cudaSuccess) return MUON_ERR_CUDA;
+    times->ms[c] += ms;
+    times->launches[c] += 1;
+  }
+  return MUON_OK;
 }
 
 muon_status muon_workspace_error(const void* workspace, void* stream, int clear, int* code) {

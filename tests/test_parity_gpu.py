@@ -255,3 +255,30 @@ def test_step_without_O_output(shape, dtype):
             # against the step that writes O: bf16 rounding of Q (2^-8 relative
             # per entry, 2^-6 allowed for sums of terms of both signs)
             assert np.linalg.norm(wf - wu) <= ulp + lrs * 2.0 ** -6 * np.linalg.norm(og), e
+
+
+def test_timed_step_gives_the_same_bits_and_kernel_times():
+    # muon_step_timed: the same kernels with an event around each launch
+    m = muon()
+    shapes = [(24, 1000), (2, 200, 150), (300, 200)]
+    W, Gs, M = make_inputs(shapes, torch.bfloat16)
+    plan = m.Plan([(s, torch.bfloat16) for s in shapes])
+    runs = []
+    for timed in (False, True):
+        Wd = [w.cuda() for w in W]; Md = [x.cuda() for x in M]
+        ws = m.alloc_workspace(plan)
+        st = m.PreparedStep(plan, Wd, [g.cuda() for g in Gs[0]], Md, workspace=ws,
+                            lr=HP["lr"], beta=HP["beta"], wd=HP["wd"], nesterov=HP["nesterov"],
+                            ns_steps=HP["ns_steps"], coeffs=HP["coeffs"])
+        t = st.timed() if timed else st()
+        torch.cuda.synchronize()
+        assert m.workspace_error(ws) == 0
+        runs.append((Wd, Md, t))
+    assert all(torch.equal(a, b) for a, b in zip(runs[0][0], runs[1][0]))
+    assert all(torch.equal(a, b) for a, b in zip(runs[0][1], runs[1][1]))
+    t = runs[1][2]
+    # one fused launch; per dense group front, finalize + normalize, 3 x 5 products
+    assert t["skinny"][1] == 1 and t["front"][1] == 2 and t["norm"][1] == 4
+    assert t["gemm"][1] == 30 and t["update"][1] == 0 and t["check"][1] == 0
+    assert all(t[k][0] > 0 for k in ("skinny", "front", "norm", "gemm"))
+    assert sum(t[k][1] for k in t) == plan.launches(HP["ns_steps"])
