@@ -393,6 +393,29 @@ def run_ours(args, w):
     ms = max_over_ranks(sum(per) / len(per), dev)
     err = mu.workspace_error(wsp, stream)
 
+    # ---- the step with the write-back of its dirty L2 lines: the flush that
+    # precedes a step also writes back what the previous step left dirty in
+    # L2 (its M' and W'), so time [flush + step] and subtract the time of a
+    # flush of a clean L2 (one right after another flush)
+    n_wb = max(1, min(args.steps, 20))
+    wb, clean = [], []
+    for _ in range(n_wb):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        flush.zero_()
+        step()
+        b.record(stream)
+        c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        c.record(stream)
+        flush.zero_()
+        d.record(stream)
+        wb.append((a, b))
+        clean.append((c, d))
+    torch.cuda.synchronize(dev)
+    ms_wb = max_over_ranks(statistics.mean(x.elapsed_time(y) for x, y in wb) -
+                           statistics.mean(x.elapsed_time(y) for x, y in clean), dev)
+
     # ---- per-kernel device time: the same step through muon_step_timed, a
     # CUDA event on the launching stream before every launch (a second timed
     # region right after the first, L2 flushed before each step)
@@ -461,6 +484,7 @@ def run_ours(args, w):
         roof = {"bound": "hbm", "kernel": "skinny_kernel", "achieved": achieved,
                 "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
                 "traffic": traffic,
+                "frac_with_writeback": nbytes / (ms_wb * 1e-3) / 1e9 / pk["hbm"],
                 "note": "algorithmic bytes %d B/element x %d elements per launch; peak %s" % (
                     per_el, w.num_elements, "of measured" if pk["src"] == "measured" else "of fallback")}
     else:
@@ -507,6 +531,7 @@ def run_ours(args, w):
     out = {"metric": METRIC, "value": weak_scaling_value(n_slices, ws_n, ms), "unit": UNIT,
            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
            "ms_per_step_median": statistics.median(per), "ms_per_step_min": min(per),
+           "ms_per_step_with_writeback": ms_wb,
            "plan_ms": statistics.median(plan_t),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": arith, "data": "synthetic",

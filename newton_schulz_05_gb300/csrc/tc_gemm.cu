@@ -529,13 +529,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // 32 KB instead of 48 KB, so six stages are in flight instead of four and a
 // CTA moves two thirds of the operand bytes per MMA flop.
 //
-// Roles per CTA (6 warps): warp 0 loads its operand halves into its own
-// stages (counted on its own `loaded` barrier, so that it can always wait
-// for its own copies); in CTA 1, warp 1 relays each landed stage to CTA 0
-// (remote arrive on CTA 0's `ready` barrier); in CTA 0, warp 1 issues the
-// pair's MMAs once both halves of a stage are in and releases stages and
-// accumulators to both CTAs by multicast commits; warps 2-5 of both CTAs run
-// the epilogue of their 128 rows and report to CTA 0's `tempty` barrier.
+// Roles per CTA (6 warps): warp 0 loads this CTA's operand halves into its
+// own stages; the copies of both CTAs complete on CTA 0's `loaded` barrier,
+// which CTA 0's producer arms with the bytes of both halves.  In CTA 0,
+// warp 1 issues the pair's MMAs and releases stages and accumulators to both
+// CTAs by multicast commits.  Warps 2-5 of both CTAs run the epilogue of
+// their 128 rows and report to CTA 0's `tempty` barrier.
+//
+// Draining: CTA 1 cannot watch the barrier its copies complete on, so when
+// its producer stops it stores how many stages it issued into CTA 0's
+// shared memory and arrives on CTA 0's `peer_done`; CTA 0's producer then
+// waits until every stage either CTA issued has landed (arming the stages
+// only CTA 1 issued with CTA 1's bytes, and completing, for stages only CTA
+// 0 issued, the bytes CTA 1 never sent) and arrives on CTA 1's `drained`.
+// No CTA leaves with a copy in flight.
 constexpr int PSTAGES = 6;
 constexpr int B_HALF = 128 * BK * 2;               // 16 KB: this CTA's half of B
 constexpr int PSTAGE_BYTES = A_BYTES + B_HALF;     // 32 KB
@@ -555,25 +562,25 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
                    : "memory");
 }
-// bounded wait at cluster scope (the phase may be completed from the peer CTA)
-__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity,
-                                             uint32_t limit = kWaitLimit) {
-  const uint32_t a = smem_u32(bar);
-  for (uint32_t i = 0; i < limit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
+// arrive on a barrier of another CTA of the cluster (shared::cluster address)
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr)
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
+}
+// the barrier's pending transaction count drops by `bytes` (bytes that will
+// never arrive)
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on a
+// barrier of CTA 0 of the pair (shared::cluster address)
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t bar0,
+                                                 int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar0), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
 }
 __device__ __forceinline__ void mma2_f16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -622,25 +629,30 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* epi = smem + PSTAGES * PSTAGE_BYTES;    // 4 x EPI_BYTES staging
-  uint64_t* loaded = reinterpret_cast<uint64_t*>(epi + 4 * EPI_BYTES);  // own stage landed
-  uint64_t* ready = loaded + PSTAGES;    // CTA 0: the peer's stage landed (relayed)
-  uint64_t* empty = ready + PSTAGES;     // stage free (multicast commit)
+  uint64_t* loaded = reinterpret_cast<uint64_t*>(epi + 4 * EPI_BYTES);  // CTA 0: both halves in
+  uint64_t* empty = loaded + PSTAGES;    // stage free (multicast commit)
   uint64_t* tfull = empty + PSTAGES;     // accumulator ready (multicast commit)
   uint64_t* tempty = tfull + 2;          // CTA 0: accumulator drained by all 8 epilogue warps
   uint64_t* mdrain = tempty + 2;         // CTA 0: every MMA issued has completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdrain + 1);
+  uint64_t* peer_done = mdrain + 1;      // CTA 0: CTA 1's producer has stopped
+  uint64_t* drained = peer_done + 1;     // CTA 1: every copy of the pair has landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);  // CTA 0
+  volatile int* skip_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);  // CTA 1: from CTA 0
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < PSTAGES; ++s) {
-      mbar_init(&loaded[s], 1); mbar_init(&ready[s], 1); mbar_init(&empty[s], 1);
-    }
+    for (int s = 0; s < PSTAGES; ++s) { mbar_init(&loaded[s], 1); mbar_init(&empty[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 8); }
     mbar_init(mdrain, 1);
+    mbar_init(peer_done, 1);
+    mbar_init(drained, 1);
     *abort_flag = 0;
+    *peer_issued = 0;
+    *skip_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
@@ -653,12 +665,24 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();   // barriers of both CTAs initialised before any remote arrive
+  cluster_sync_all();   // barriers of both CTAs initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int kblocks = p.K / BK;
   pdl_wait();
-  const bool skipped = (p.skip && *p.skip) || *static_cast<volatile int*>(p.err) != 0;
+  // CTA 0 decides for the pair whether the step is skipped (a skipped
+  // loss-scaled step, or a wait of the step that gave up), so that both
+  // CTAs take the same path
+  if (rank == 0 && threadIdx.x == 0) {
+    const int sk = (p.skip && *p.skip) || *static_cast<volatile int*>(p.err) != 0;
+    asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(
+                     mapa(smem_u32(const_cast<int*>(skip_flag)), 1)),
+                 "r"(sk)
+                 : "memory");
+    *skip_flag = sk;
+  }
+  cluster_sync_all();
+  const bool skipped = *skip_flag != 0;
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -669,64 +693,84 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // no role runs; only the teardown below
   } else if (warp == 0) {
     if (lane == 0) {
-      // producer: this CTA's halves of every stage, on its own barrier
+      // producer: this CTA's halves of every stage
       uint32_t it = 0;
       for (int t = pair; t < p.total_tiles && !*abort_flag; t += npairs) {
         int b, I2, J;
         pair_tile_coords(p, t, b, I2, J);
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % PSTAGES;
-          const uint32_t ph = (it / PSTAGES) & 1;
-          if (!mbar_wait_cl(&empty[s], ph ^ 1, p.wait_limit)) { fail(); break; }
-          unsigned char* sa = smem + s * PSTAGE_BYTES;
-          unsigned char* sb = sa + A_BYTES;
-          mbar_expect_tx(&loaded[s], PSTAGE_BYTES);
-          tma_load_3d(sa, &tmA, &loaded[s], kb * BK, I2 * 256 + (int)rank * 128, b);
-          if (!p.b_mn) {
-            tma_load_3d(sb, &tmB, &loaded[s], kb * BK, J * 256 + (int)rank * 128, b);
-          } else {
-            #pragma unroll
-            for (int q = 0; q < 2; ++q)
-              tma_load_3d(sb + q * (64 * BK * 2), &tmB, &loaded[s], J * 256 + (int)rank * 128 + q * 64,
-                          kb * BK, b);
-          }
-        }
-      }
-      // every issued load lands before the CTA may leave
-      const uint32_t last = it;
-      for (uint32_t k = (last > PSTAGES ? last - PSTAGES : 0); k < last; ++k)
-        if (!mbar_wait(&loaded[k % PSTAGES], (k / PSTAGES) & 1)) { fail(); break; }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && rank == 1) {
-      // relay: each stage of this CTA that has landed is reported to CTA 0
-      uint32_t it = 0;
-      for (int t = pair; t < p.total_tiles && !*abort_flag; t += npairs) {
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % PSTAGES;
           const uint32_t ph = (it / PSTAGES) & 1;
-          if (!mbar_wait(&loaded[s], ph, p.wait_limit)) { fail(); ok = false; break; }
-          mbar_arrive_remote(mapa(smem_u32(&ready[s]), 0));
+          if (!mbar_wait(&empty[s], ph ^ 1, p.wait_limit)) { fail(); ok = false; break; }
+          unsigned char* sa = smem + s * PSTAGE_BYTES;
+          unsigned char* sb = sa + A_BYTES;
+          const int row = I2 * 256 + (int)rank * 128;
+          const int col = J * 256 + (int)rank * 128;
+          if (rank == 0) {
+            mbar_expect_tx(&loaded[s], 2 * PSTAGE_BYTES);   // both halves
+            tma_load_3d(sa, &tmA, &loaded[s], kb * BK, row, b);
+            if (!p.b_mn) {
+              tma_load_3d(sb, &tmB, &loaded[s], kb * BK, col, b);
+            } else {
+              #pragma unroll
+              for (int q = 0; q < 2; ++q)
+                tma_load_3d(sb + q * (64 * BK * 2), &tmB, &loaded[s], col + q * 64, kb * BK, b);
+            }
+          } else {
+            const uint32_t bar0 = mapa(smem_u32(&loaded[s]), 0);
+            tma_load_3d_pair(sa, &tmA, bar0, kb * BK, row, b);
+            if (!p.b_mn) {
+              tma_load_3d_pair(sb, &tmB, bar0, kb * BK, col, b);
+            } else {
+              #pragma unroll
+              for (int q = 0; q < 2; ++q)
+                tma_load_3d_pair(sb + q * (64 * BK * 2), &tmB, bar0, col + q * 64, kb * BK, b);
+            }
+          }
         }
         if (!ok) break;
       }
-    } else if (lane == 0) {
+      if (rank == 1) {
+        // report the stages issued, then wait until CTA 0 has seen them land
+        asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(
+                         mapa(smem_u32(const_cast<uint32_t*>(peer_issued)), 0)),
+                     "r"(it)
+                     : "memory");
+        asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
+        mbar_arrive_remote(mapa(smem_u32(peer_done), 0));
+        if (!mbar_wait(drained, 0)) fail();
+      } else {
+        if (!mbar_wait(peer_done, 0)) {
+          fail();
+        } else {
+          asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
+          const uint32_t it1 = *peer_issued;
+          const uint32_t hi = it > it1 ? it : it1;
+          for (uint32_t k = (hi > PSTAGES ? hi - PSTAGES : 0); k < hi; ++k) {
+            uint64_t* bar = &loaded[k % PSTAGES];
+            if (k >= it) mbar_expect_tx(bar, PSTAGE_BYTES);       // CTA 1's half only
+            else if (k >= it1) mbar_complete_tx(bar, PSTAGE_BYTES);  // CTA 1 never sent its half
+            if (!mbar_wait(bar, (k / PSTAGES) & 1)) { fail(); break; }
+          }
+        }
+        mbar_arrive_remote(mapa(smem_u32(drained), 1));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
       // CTA 0: the pair's MMAs (M = 256, N = 256, K = 16)
       uint32_t it = 0, tl = 0;
       for (int t = pair; t < p.total_tiles && !*abort_flag; t += npairs, ++tl) {
         const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
-        if (!mbar_wait_cl(&tempty[acc], aph ^ 1, p.wait_limit)) { fail(); break; }
+        if (!mbar_wait(&tempty[acc], aph ^ 1, p.wait_limit)) { fail(); break; }
         tc_fence_after();
         const uint32_t dt = tmem + acc * BN;
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % PSTAGES;
           const uint32_t ph = (it / PSTAGES) & 1;
-          if (!mbar_wait(&loaded[s], ph, p.wait_limit) ||
-              !mbar_wait_cl(&ready[s], ph, p.wait_limit)) {
-            fail(); ok = false; break;
-          }
+          if (!mbar_wait(&loaded[s], ph, p.wait_limit)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * PSTAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
@@ -757,7 +801,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int b, I2, J;
       pair_tile_coords(p, t, b, I2, J);
       const uint32_t acc = tl & 1, aph = (tl >> 1) & 1;
-      if (!mbar_wait_cl(&tfull[acc], aph, p.wait_limit)) { fail(); break; }
+      if (!mbar_wait(&tfull[acc], aph, p.wait_limit)) { fail(); break; }
       tc_fence_after();
       const int I = 2 * I2 + (int)rank;    // 128-row block of this CTA
       if (I * BM < p.M)                    // past M: rows of zeros, nothing to store
@@ -772,7 +816,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();   // the peer's MMAs and remote arrives are done with this CTA
+  cluster_sync_all();   // the peer's MMAs and remote accesses are done with this CTA
   tc_fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
