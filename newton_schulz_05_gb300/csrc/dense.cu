@@ -332,18 +332,31 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   if constexpr (sizeof(IT) == 2) {
     // fp16 operands: the three products on the tcgen05 tensor cores.  The
     // a and b terms of the step are folded into the operands, so that no
-    // product reads a third matrix:  b A + c A A = A (c A + b I)  and
-    // a X + B X = (B + a I) X.  Padded rows and columns of X are zero, so the
-    // identity entries past m meet only zeros.
+    // product reads a third matrix, and a X + B X = (B + a I) X.  Padded rows
+    // and columns of X are zero, so the identity entries past m meet only
+    // zeros.  The polynomial B + a I = c A A + b A + a I is formed from one
+    // matrix when that is numerically safe:
+    //   Y = c A + (b/2) I  (the Gram's only output),
+    //   B + a I = Y Y / c + (a - b^2 / (4c)) I;
+    // the constant b^2 / (4c) is 2.8 for the default coefficients against
+    // a = 3.4 (CPU emulation: the same error as the two-output form).  When
+    // b^2 / (4|c|) is large against the coefficients (or c = 0) the Gram
+    // writes A and A2 = c A + b I instead and the product is A A2 + a I.
+    const float ab = fabsf(st.b), ac = fabsf(st.c);
+    const bool yform = st.c != 0.f && st.b * st.b / (4.f * ac) <= 2.9f * (1.45f * ac + ab);
     for (int t = 0; t < st.T; ++t) {
       const bool last = t == st.T - 1;
       TcGemm g1;
       g1.batch = ns; g1.stride = sws; g1.err = err_word; g1.skip = st.skip;
       g1.wait_limit = st.wait_limit;
-      // A = X X^T and A2 = c X X^T + b I (symmetric)
+      // Y = c X X^T + (b/2) I, or A = X X^T and A2 = c X X^T + b I (symmetric)
       g1.M = mp; g1.N = mp; g1.K = np;
       g1.A = ws + xin; g1.B = ws + xin; g1.D = ws + off.A; g1.sym = 1;
-      g1.D2 = ws + off.A2; g1.alpha2 = st.c; g1.diag2 = st.b;
+      if (yform) {
+        g1.alpha = st.c; g1.diag = 0.5f * st.b;      // Y = c X X^T + (b/2) I
+      } else {
+        g1.D2 = ws + off.A2; g1.alpha2 = st.c; g1.diag2 = st.b;
+      }
       cudaError_t e;
       {
         NvtxRange r("muon::tc_gemm gram");
@@ -351,13 +364,21 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
         e = tc_gemm(g1, s);
       }
       if (e != cudaSuccess) return e;
-      // B' = A A2 + a I = b A + c A A + a I (symmetric: A and A2 commute)
+      // B' = b A + c A A + a I (symmetric), as Y Y / c + (a - b^2/(4c)) I or
+      // as A A2 + a I (A and A2 commute)
       TcGemm g2;
       g2.batch = ns; g2.stride = sws; g2.err = err_word; g2.skip = st.skip;
       g2.wait_limit = st.wait_limit;
       g2.M = mp; g2.N = mp; g2.K = mp;
-      g2.A = ws + off.A; g2.B = ws + off.A2; g2.D = ws + off.B; g2.sym = 1;
-      g2.diag = st.a;
+      if (yform) {
+        // B' = Y Y / c + (a - b^2 / (4c)) I
+        g2.A = ws + off.A; g2.B = ws + off.A; g2.D = ws + off.B; g2.sym = 1;
+        g2.alpha = 1.f / st.c;
+        g2.diag = st.a - st.b * st.b / (4.f * st.c);
+      } else {
+        g2.A = ws + off.A; g2.B = ws + off.A2; g2.D = ws + off.B; g2.sym = 1;
+        g2.diag = st.a;
+      }
       {
         NvtxRange r("muon::tc_gemm poly");
         st.mark(MUON_KC_GEMM);
