@@ -169,22 +169,39 @@ class ClockSampler:
                 "sm_max_mhz": num(rows[0][2]), "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def skinny_traffic(per_launch_units):
-    """DRAM bytes of one fused-kernel launch from the committed ncu summary,
-    valid only while the kernel source is unchanged."""
-    path = os.path.join(ROOT, "profiles", "skinny_kernel_74x24x10240.txt")
-    src = os.path.join(ROOT, "newton_schulz_05_gb300", "csrc", "skinny.cu")
+def source_digest(path: str) -> str:
+    """sha256 of a C/C++/CUDA source with its comments and blank space
+    removed, so that an edit of comments alone keeps a profile valid while
+    any change of code invalidates it."""
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = " ".join(text.split())
+    return hashlib.sha256(text.encode()).hexdigest()
+
+
+def profile_value(profile: str, source: str, key: str):
+    """A number from a committed ncu summary, valid only while the kernel
+    source it was captured from is unchanged (by source_digest)."""
+    path = os.path.join(ROOT, "profiles", profile)
+    src = os.path.join(ROOT, "newton_schulz_05_gb300", "csrc", source)
     if not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     kv = {}
     for line in open(path):
         if ":" in line:
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("skinny.cu sha256") != sha or "dram bytes per launch" not in kv:
+    if kv.get("source digest") != source_digest(src) or key not in kv:
         return None
-    return float(kv["dram bytes per launch"])
+    return float(kv[key].split()[0])
+
+
+def skinny_traffic(per_launch_units):
+    """DRAM bytes of one fused-kernel launch of the 74 x [24, 10240] workload
+    from the committed ncu summary, while skinny.cu is unchanged."""
+    return profile_value("skinny_kernel_74x24x10240.txt", "skinny.cu", "dram bytes per launch")
 
 
 # ---------------------------------------------------------------- oracle leg

@@ -48,3 +48,30 @@ def test_peaks_come_from_the_measured_file_when_present():
     pk = bench.peaks()
     assert pk["src"] in ("measured", "fallback")
     assert pk["hbm"] > 1000 and pk["tc"] > pk["tc_sustained"] > 100
+
+
+def test_source_digest_ignores_comments_only(tmp_path):
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("// header\nint f(int x) {  /* twice */ return 2 * x; }\n")
+    b = tmp_path / "b.cu"
+    b.write_text("/* another\n header */\nint f(int x) {\n  return 2 * x;  // doubled\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) { return 3 * x; }\n")
+    assert bench.source_digest(str(a)) == bench.source_digest(str(b))
+    assert bench.source_digest(str(a)) != bench.source_digest(str(c))
+
+
+def test_profile_value_needs_a_matching_digest(tmp_path, monkeypatch):
+    import bench
+    prof = tmp_path / "profiles"
+    src = tmp_path / "newton_schulz_05_gb300" / "csrc"
+    prof.mkdir()
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text("__global__ void k() {}\n")
+    digest = bench.source_digest(str(src / "k.cu"))
+    (prof / "k.txt").write_text("source digest: %s\ndram bytes per launch: 1234\n" % digest)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profile_value("k.txt", "k.cu", "dram bytes per launch") == 1234.0
+    (src / "k.cu").write_text("__global__ void k() { int x = 0; }\n")
+    assert bench.profile_value("k.txt", "k.cu", "dram bytes per launch") is None
