@@ -410,28 +410,33 @@ def run_ours(args, w):
     ms = max_over_ranks(sum(per) / len(per), dev)
     err = mu.workspace_error(wsp, stream)
 
-    # ---- the step with the write-back of its dirty L2 lines: the flush that
-    # precedes a step also writes back what the previous step left dirty in
-    # L2 (its M' and W'), so time [flush + step] and subtract the time of a
-    # flush of a clean L2 (one right after another flush)
+    # ---- the step with the write-back of its dirty L2 lines.  A read-only
+    # sweep over a buffer larger than L2 evicts every line and writes back
+    # the dirty ones without leaving new dirty lines.  Per iteration: flush
+    # and sweep (L2 clean, none of the step's data cached), then the step,
+    # then a sweep (which writes back what the step left dirty), then a
+    # second sweep (nothing left to write back); the step with its
+    # write-back is step + first sweep - second sweep.
+    sweep_buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     n_wb = max(1, min(args.steps, 20))
-    wb, clean = [], []
+    marks = []
     for _ in range(n_wb):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
         flush.zero_()
+        sweep_buf.sum()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
         step()
-        b.record(stream)
-        c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        flush.zero_()
-        c.record(stream)
-        flush.zero_()
-        d.record(stream)
-        wb.append((a, b))
-        clean.append((c, d))
+        e[1].record(stream)
+        sweep_buf.sum()
+        e[2].record(stream)
+        sweep_buf.sum()
+        e[3].record(stream)
+        marks.append(e)
     torch.cuda.synchronize(dev)
-    ms_wb = max_over_ranks(statistics.mean(x.elapsed_time(y) for x, y in wb) -
-                           statistics.mean(x.elapsed_time(y) for x, y in clean), dev)
+    ms_wb = max_over_ranks(statistics.mean(
+        e[0].elapsed_time(e[1]) + e[1].elapsed_time(e[2]) - e[2].elapsed_time(e[3])
+        for e in marks), dev)
+    del sweep_buf
 
     # ---- per-kernel device time: the same step through muon_step_timed, a
     # CUDA event on the launching stream before every launch (a second timed
