@@ -451,11 +451,13 @@ def run_ours(args, w):
     kernels = {k: {"ms_per_step": v[0] / n_timed, "launches_per_step": v[1] / n_timed}
                for k, v in acc.items() if v[1]}
 
-    # ---- end to end through the public API, host buffers (pinned).  Each
-    # kind of state (parameters, gradients, momentum) lives in one flat
-    # buffer on either side, the parameters being views into it (the layout
-    # of a flat-parameter data-parallel trainer), so a step moves it with one
-    # copy per kind and direction.
+    # ---- end to end through the public API with HOST buffers: the optimizer
+    # state (parameters, gradients, momenta) in page-locked host memory, one
+    # muon_step_host call per step, which copies each unit of slices in,
+    # steps it and copies its parameters and momenta back, copies
+    # overlapping the kernels.  Each kind of state lives in one flat host
+    # buffer, the parameters being views into it (the layout of a
+    # flat-parameter data-parallel trainer).
     def flat(ts, device, pin=False):
         buf = torch.empty(sum(x.numel() for x in ts), dtype=ts[0].dtype, device=device,
                           pin_memory=pin)
@@ -470,31 +472,27 @@ def run_ours(args, w):
     hM, Mh = flat(M, "cpu", True)
     for d, h in zip(W + G + M, Wh + Gh + Mh):
         h.copy_(d)
-    dW, Wd = flat(W, dev)
-    dG, Gd = flat(G, dev)
-    dM, Md = flat(M, dev)
     h2d = sum(x.numel() * x.element_size() for x in (hW, hG, hM))
     d2h = sum(x.numel() * x.element_size() for x in (hW, hM))
-    opt_step = mu.PreparedStep(plan, Wd, Gd, Md, workspace=wsp, stream=stream, **hp)
-
-    def e2e_step():
-        for d, h in ((dW, hW), (dG, hG), (dM, hM)):
-            d.copy_(h, non_blocking=True)
-        opt_step()
-        for d, h in ((dW, hW), (dM, hM)):
-            h.copy_(d, non_blocking=True)
+    # three staging buffers of about an eighth of the state each, at most 2 GB
+    part = max(plan.host_staging_bytes // 3, min(2 << 30, h2d // 8))
+    staging = torch.empty(3 * part + 256, dtype=torch.uint8, device=dev)
+    del W, G, M, step   # the device copies are not needed any more
+    host_step = mu.PreparedHostStep(plan, Wh, Gh, Mh, workspace=wsp, staging=staging,
+                                    stream=stream, **hp)
 
     for _ in range(min(args.warmup, 3)):
-        e2e_step()
+        host_step()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_steps = max(1, min(args.steps, 50))
     e0.record(stream)
     for _ in range(e_steps):
-        e2e_step()
+        host_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
+    assert mu.workspace_error(wsp, stream) == 0
 
     nbytes, flops, flops_sym, skinny_bytes, per_el = workload_work(w)
     pk = peaks()
@@ -563,6 +561,11 @@ def run_ours(args, w):
                       "mode": mode},
            "roofline": roof, "kernels": kernels,
            "e2e": {"value": weak_scaling_value(n_slices, ws_n, ms_e2e), "unit": UNIT,
+                   "ms_per_step": ms_e2e,
+                   "call": "muon_step_host: parameters, gradients and momenta in page-locked "
+                           "host memory; per step every unit of slices is copied in, stepped "
+                           "and its parameters and momenta copied back, the copies of one unit "
+                           "overlapping the kernels of its neighbours",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
            "clocks": clocks, "gpu_launches": launches_per_step * args.steps,
            "wall_s_timed": t_wall, "device_error": err}

@@ -305,6 +305,38 @@ MUON_API muon_status muon_step_timed(const muon_plan_t* plan, void* const* param
                                      const float* coeffs, void* workspace, size_t ws_bytes,
                                      void* stream, muon_kernel_times* times);
 
+/*
+ * muon_step on parameters, gradients and momenta held in HOST memory (an
+ * optimizer whose state lives in host memory; on a Grace-Blackwell node the
+ * GPU reaches it over NVLink-C2C).  The plan's slices are cut into units of
+ * whole slices that fit a third of `staging`; each unit's parameters,
+ * gradients and momenta are copied to the device, stepped by the kernels of
+ * muon_step, and its parameters and momenta copied back, the copies of one
+ * unit overlapping the kernels of its neighbours (three staging buffers in
+ * rotation, two copy streams of the call's own).
+ *   params, grads, momentum  host pointers (page-locked memory gives full
+ *                            copy bandwidth; pageable memory works, slower),
+ *                            shapes and dtypes as for muon_step
+ *   workspace, ws_bytes      device, as for muon_step
+ *   staging, staging_bytes   device, 256-byte aligned, at least
+ *                            muon_plan_host_staging_bytes; larger staging
+ *                            gives larger units (fewer launches) and a longer
+ *                            pipeline fill and drain
+ * Asynchronous: the work is ordered before any later work on `stream`;
+ * synchronise `stream` before reading the host buffers.  Returns
+ * MUON_ERR_WORKSPACE when one slice does not fit a third of the staging.
+ * Other arguments are those of muon_step.  The RFC has no counterpart of
+ * this call.
+ */
+MUON_API muon_status muon_step_host(const muon_plan_t* plan, void* const* params,
+                                    const void* const* grads, float* const* momentum, float lr,
+                                    float beta, float wd, int nesterov, int ns_steps,
+                                    const float* coeffs, void* workspace, size_t ws_bytes,
+                                    void* staging, size_t staging_bytes, void* stream);
+/* smallest staging for muon_step_host: three copies of the largest slice's
+ * parameter, gradient and momentum (host only, no device call) */
+MUON_API muon_status muon_plan_host_staging_bytes(const muon_plan_t* plan, size_t* out);
+
 /* Kernel launches muon_step makes for this plan and ns_steps, for a step
  * without O outputs (for accounting; no device call). */
 MUON_API muon_status muon_plan_launches(const muon_plan_t* plan, int ns_steps, int* out);

@@ -70,7 +70,7 @@ EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
            "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
            "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static",
            "muon_step_amp", "muon_adamw_step", "muon_plan_partition", "muon_static_error",
-           "muon_step_timed"]
+           "muon_step_timed", "muon_step_host", "muon_plan_host_staging_bytes"]
 
 STATIC_WORKSPACE_BYTES = 32 << 20   # MUON_STATIC_WORKSPACE_BYTES in include/muon.h
 
@@ -108,6 +108,8 @@ def load(path: str = LIB_PATH):
     L.muon_step.argtypes = step_args
     L.muon_step_ortho.argtypes = step_args + [PP]
     L.muon_step_timed.argtypes = step_args + [ctypes.POINTER(_KernelTimes)]
+    L.muon_step_host.argtypes = step_args[:12] + [vp, sz, vp]
+    L.muon_plan_host_staging_bytes.argtypes = [vp, ctypes.POINTER(sz)]
     L.muon_step_static.argtypes = step_args[:10] + [vp]
     L.muon_step_amp.argtypes = step_args[:10] + [ctypes.c_float, vp, vp, sz, vp]
     L.muon_adamw_step.argtypes = [ctypes.c_int, PP, PP, PP, PP, ctypes.POINTER(ctypes.c_int64),
@@ -127,7 +129,8 @@ def load(path: str = LIB_PATH):
                "muon_plan_num_slices", "muon_plan_group", "muon_plan_slice", "muon_step",
                "muon_step_ortho", "muon_workspace_error", "muon_plan_launches",
                "muon_step_static", "muon_step_amp", "muon_adamw_step", "muon_plan_partition",
-               "muon_static_error", "muon_step_timed"):
+               "muon_static_error", "muon_step_timed", "muon_step_host",
+               "muon_plan_host_staging_bytes"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -218,6 +221,13 @@ class Plan:
         _check(load().muon_plan_slice(self._h, param, e, ctypes.byref(g), ctypes.byref(i)),
                "plan_slice")
         return g.value, i.value
+
+    @property
+    def host_staging_bytes(self) -> int:
+        """Smallest device staging buffer of muon_step_host for this plan."""
+        v = ctypes.c_size_t()
+        _check(load().muon_plan_host_staging_bytes(self._h, ctypes.byref(v)), "host_staging_bytes")
+        return v.value
 
     def launches(self, ns_steps: int = 5) -> int:
         v = ctypes.c_int()
@@ -432,6 +442,44 @@ class PreparedStep:
         t = _KernelTimes()
         _check(load().muon_step_timed(*self._args, ctypes.byref(t)), "muon_step_timed")
         return {k: (t.ms[i], t.launches[i]) for i, k in enumerate(KERNEL_CLASSES)}
+
+
+class PreparedHostStep:
+    """A muon_step_host call (parameters, gradients and momenta in host
+    memory, streamed through a device staging buffer) with its argument
+    arrays marshalled once.  params/grads/momentum: CPU tensors, contiguous
+    (page-locked for full copy bandwidth); the call updates params and
+    momentum in place once the stream has run it."""
+
+    def __init__(self, plan: Plan, params, grads, momentum, *, lr: float, beta: float, wd: float,
+                 nesterov: bool = True, ns_steps: int = 5, coeffs=DEFAULT_COEFFS,
+                 workspace: torch.Tensor, staging: torch.Tensor, stream=None):
+        n = len(plan.shapes)
+        if not (len(params) == len(grads) == len(momentum) == n):
+            raise ValueError("expected %d params, grads and momentum tensors" % n)
+        for i, (p, g, m) in enumerate(zip(params, grads, momentum)):
+            if tuple(p.shape) != plan.shapes[i] or g.shape != p.shape or m.shape != p.shape:
+                raise ValueError("tensor %d does not match the plan's shape" % i)
+            if _DTYPES.get(p.dtype) != plan.dtypes[i] or g.dtype != p.dtype or m.dtype != torch.float32:
+                raise TypeError("tensor %d: dtype mismatch with the plan" % i)
+            if p.is_cuda or g.is_cuda or m.is_cuda or not (p.is_contiguous() and g.is_contiguous()
+                                                          and m.is_contiguous()):
+                raise ValueError("tensor %d must be a contiguous host tensor" % i)
+        if not staging.is_cuda or staging.data_ptr() % 256:
+            raise ValueError("staging must be a 256-byte aligned CUDA buffer")
+        self._keep = (plan, list(params), list(grads), list(momentum), workspace, staging)
+        c = (ctypes.c_float * 3)(*coeffs)
+        self._args = [plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum),
+                      ctypes.c_float(lr), ctypes.c_float(beta), ctypes.c_float(wd),
+                      ctypes.c_int(int(bool(nesterov))), ctypes.c_int(ns_steps), c,
+                      ctypes.c_void_p(workspace.data_ptr()),
+                      ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                      ctypes.c_void_p(staging.data_ptr()),
+                      ctypes.c_size_t(staging.numel() * staging.element_size()),
+                      ctypes.c_void_p(_stream_handle(stream))]
+
+    def __call__(self) -> None:
+        _check(load().muon_step_host(*self._args), "muon_step_host")
 
 
 class Partition:

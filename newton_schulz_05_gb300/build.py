@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmuon.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["plan.cpp", "step.cu", "dense.cu", "skinny.cu", "tc_gemm.cu", "noalloc.cu", "adamw.cu"]
+SOURCES = ["plan.cpp", "step.cu", "dense.cu", "skinny.cu", "tc_gemm.cu", "noalloc.cu", "adamw.cu",
+           "host.cu"]
 
 
 def _nvcc() -> str:

@@ -1,0 +1,221 @@
+// muon_step_host: one Muon step on parameters, gradients and momenta held in
+// host memory.  The optimizer state of a large model can live in host memory
+// (on a Grace-Blackwell node the GPU reaches it over NVLink-C2C); the step
+// then streams it through a device staging buffer.
+//
+// The plan's slices are cut into units that fit a third of the staging
+// buffer (whole slices of one group, at most a dense chunk or one fused
+// launch).  Unit k is copied in on its own stream, stepped on the caller's
+// stream and copied out on a third stream, in buffer third k % 3, so the
+// copies of one unit overlap the kernels of its neighbours:
+//
+//   h2d stream   [in 0][in 1]      [in 2]      [in 3] ...
+//   caller       .     [step 0]    [step 1]    [step 2] ...
+//   d2h stream   .     .           [out 0]     [out 1] ...
+//
+// Buffer k % 3 takes unit k + 3 once unit k has been copied out, so the
+// kernels never wait as long as a unit's copies in and out take together at
+// most about twice as long as its kernels.
+//
+// A unit's parameters, gradients and momenta go in (2 + 2 + 4 bytes per bf16
+// element); its parameters and momenta come back (2 + 4).  Contiguous slices
+// of one parameter move in one copy.
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "internal.h"
+
+using namespace muon;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kBufs = 3;   // staging buffers in rotation
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Unit {
+  int group;
+  int i0, i1;                   // slices [i0, i1) of the group, in group order
+  size_t bytes;                 // staging bytes (W, G and M regions)
+};
+
+// staging bytes of one slice of group g: W, G and M, each 256-byte aligned
+size_t slice_stage_bytes(const Group& g) {
+  const size_t es = g.dtype == MUON_BF16 ? 2 : 4;
+  const size_t mn = (size_t)g.M * (size_t)g.N;
+  return 2 * align_up(mn * es) + align_up(mn * 4);
+}
+
+muon_status make_units(const muon_plan_t* P, size_t part, std::vector<Unit>& units) {
+  for (int gi = 0; gi < (int)P->groups.size(); ++gi) {
+    const Group& g = P->groups[gi];
+    const size_t per = slice_stage_bytes(g);
+    if (per > part) return MUON_ERR_WORKSPACE;
+    const int cap_n = g.kernel == MUON_KERNEL_SKINNY ? kMaxSlicesPerLaunch : g.chunk;
+    int fit = (int)std::min<size_t>(part / per, (size_t)cap_n);
+    if (fit < 1) fit = 1;
+    for (int i0 = 0; i0 < g.count(); i0 += fit) {
+      const int i1 = std::min(g.count(), i0 + fit);
+      units.push_back(Unit{gi, i0, i1, per * (size_t)(i1 - i0)});
+    }
+  }
+  return MUON_OK;
+}
+
+struct Copy {
+  void* dst;
+  const void* src;
+  size_t bytes;
+};
+
+// one copy per run of slices that are contiguous on both sides
+void add_run(std::vector<Copy>& v, void* dst, const void* src, size_t bytes, bool merge) {
+  if (merge && !v.empty() && static_cast<char*>(v.back().dst) + v.back().bytes == dst &&
+      static_cast<const char*>(v.back().src) + v.back().bytes == src) {
+    v.back().bytes += bytes;
+    return;
+  }
+  v.push_back(Copy{dst, src, bytes});
+}
+
+}  // namespace
+
+extern "C" muon_status muon_plan_host_staging_bytes(const muon_plan_t* P, size_t* out) {
+  if (!P || !out) return MUON_ERR_INVALID_ARG;
+  size_t m = 0;
+  for (const Group& g : P->groups) m = std::max(m, slice_stage_bytes(g));
+  *out = kBufs * m;
+  return MUON_OK;
+}
+
+extern "C" muon_status muon_step_host(const muon_plan_t* P, void* const* params,
+                                      const void* const* grads, float* const* momentum,
+                                      float lr, float beta, float wd, int nesterov, int ns_steps,
+                                      const float* coeffs, void* workspace, size_t ws_bytes,
+                                      void* staging, size_t staging_bytes, void* stream) {
+  if (!P) return MUON_ERR_INVALID_ARG;
+  const int np = (int)P->shapes.size();
+  if (np > 0 && (!params || !grads || !momentum)) return MUON_ERR_INVALID_ARG;
+  for (int p = 0; p < np; ++p)
+    if (!params[p] || !grads[p] || !momentum[p]) return MUON_ERR_INVALID_ARG;
+  if (ns_steps < 0 || ns_steps > 1000) return MUON_ERR_INVALID_ARG;
+  if (!std::isfinite(lr) || !std::isfinite(beta) || !std::isfinite(wd)) return MUON_ERR_INVALID_ARG;
+  if (!workspace || !staging) return MUON_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(staging)) & 255)
+    return MUON_ERR_ALIGNMENT;
+  if (ws_bytes < P->ws_bytes) return MUON_ERR_WORKSPACE;
+  StepArgs st;
+  st.lr = lr; st.beta = beta; st.wd = wd; st.nesterov = nesterov ? 1 : 0;
+  st.T = ns_steps;
+  st.a = coeffs ? coeffs[0] : 3.4445f;
+  st.b = coeffs ? coeffs[1] : -4.7750f;
+  st.c = coeffs ? coeffs[2] : 2.0315f;
+  if (!std::isfinite(st.a) || !std::isfinite(st.b) || !std::isfinite(st.c)) return MUON_ERR_INVALID_ARG;
+  st.eps = P->opt.eps;
+  const size_t part = (staging_bytes / kBufs) / kAlign * kAlign;
+  std::vector<Unit> units;
+  muon_status ms = make_units(P, part, units);
+  if (ms != MUON_OK) return ms;
+  const int fault = fault_switch();
+  if (fault == kFaultLaunch) return MUON_ERR_CUDA;
+  if (fault == kFaultTimeout) st.wait_limit = 0;
+  NvtxRange range("muon_step_host");
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* err_word = reinterpret_cast<int*>(ws);
+  char* body = ws + kHeaderBytes;
+  char* stage[kBufs];
+  for (int b = 0; b < kBufs; ++b) stage[b] = static_cast<char*>(staging) + (size_t)b * part;
+
+  // copy streams and events of this call, released when their work is done
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t entry = nullptr, in_done[kBufs] = {}, step_done[kBufs] = {}, out_done[kBufs] = {};
+  auto release = [&]() {
+    if (h2d) cudaStreamDestroy(h2d);
+    if (d2h) cudaStreamDestroy(d2h);
+    if (entry) cudaEventDestroy(entry);
+    for (int b = 0; b < kBufs; ++b)
+      for (cudaEvent_t e : {in_done[b], step_done[b], out_done[b]})
+        if (e) cudaEventDestroy(e);
+  };
+  bool ok = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&entry, cudaEventDisableTiming) == cudaSuccess;
+  for (int b = 0; b < kBufs && ok; ++b)
+    ok = cudaEventCreateWithFlags(&in_done[b], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&step_done[b], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&out_done[b], cudaEventDisableTiming) == cudaSuccess;
+  // the copies start after the caller's earlier work on its stream
+  ok = ok && cudaEventRecord(entry, s) == cudaSuccess &&
+       cudaStreamWaitEvent(h2d, entry, 0) == cudaSuccess &&
+       cudaStreamWaitEvent(d2h, entry, 0) == cudaSuccess;
+  if (!ok) { release(); return MUON_ERR_CUDA; }
+
+  std::vector<Copy> cin, cout;
+  SlicePtrs ptrs;
+  for (size_t k = 0; k < units.size() && ok; ++k) {
+    const Unit& u = units[k];
+    const Group& g = P->groups[u.group];
+    const int b = (int)(k % kBufs);
+    const size_t es = g.dtype == MUON_BF16 ? 2 : 4;
+    const size_t mn = (size_t)g.M * (size_t)g.N;
+    const int ns = u.i1 - u.i0;
+    char* wreg = stage[b];
+    char* greg = wreg + (size_t)ns * align_up(mn * es);
+    char* mreg = greg + (size_t)ns * align_up(mn * es);
+    // in-copies of W, G and M; out-copies of W' and M'
+    cin.clear(); cout.clear();
+    std::vector<Copy> cg, cm, ow, om;
+    const bool contig = (mn * es) % kAlign == 0 && (mn * 4) % kAlign == 0;
+    for (int j = 0; j < ns; ++j) {
+      const int p = g.slice_param[u.i0 + j];
+      const size_t e = (size_t)g.slice_e[u.i0 + j];
+      char* dw = wreg + (size_t)j * align_up(mn * es);
+      char* dg = greg + (size_t)j * align_up(mn * es);
+      float* dm = reinterpret_cast<float*>(mreg + (size_t)j * align_up(mn * 4));
+      char* hw = static_cast<char*>(params[p]) + e * mn * es;
+      const char* hg = static_cast<const char*>(grads[p]) + e * mn * es;
+      float* hm = momentum[p] + e * mn;
+      add_run(cin, dw, hw, mn * es, contig);
+      add_run(cg, dg, hg, mn * es, contig);
+      add_run(cm, dm, hm, mn * 4, contig);
+      add_run(ow, hw, dw, mn * es, contig);
+      add_run(om, hm, dm, mn * 4, contig);
+      ptrs.W[j] = dw;
+      ptrs.G[j] = dg;
+      ptrs.Mom[j] = dm;
+      ptrs.O[j] = nullptr;
+    }
+    cin.insert(cin.end(), cg.begin(), cg.end());
+    cin.insert(cin.end(), cm.begin(), cm.end());
+    cout = ow;
+    cout.insert(cout.end(), om.begin(), om.end());
+    // in: after buffer b was last copied out
+    ok = cudaStreamWaitEvent(h2d, out_done[b], 0) == cudaSuccess;
+    for (const Copy& c : cin)
+      ok = ok && cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDefault, h2d) == cudaSuccess;
+    ok = ok && cudaEventRecord(in_done[b], h2d) == cudaSuccess;
+    // step the unit on the caller's stream
+    ok = ok && cudaStreamWaitEvent(s, in_done[b], 0) == cudaSuccess;
+    if (ok) {
+      cudaError_t e;
+      if (g.kernel == MUON_KERNEL_SKINNY)
+        e = launch_skinny(g, ptrs, ns, st, err_word, s);
+      else
+        e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body, err_word, s, false);
+      ok = e == cudaSuccess;
+    }
+    ok = ok && cudaEventRecord(step_done[b], s) == cudaSuccess;
+    // out: after the unit's step
+    ok = ok && cudaStreamWaitEvent(d2h, step_done[b], 0) == cudaSuccess;
+    for (const Copy& c : cout)
+      ok = ok && cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDefault, d2h) == cudaSuccess;
+    ok = ok && cudaEventRecord(out_done[b], d2h) == cudaSuccess;
+  }
+  // the caller's stream continues after every copy out
+  for (int b = 0; b < kBufs && ok; ++b) ok = cudaStreamWaitEvent(s, out_done[b], 0) == cudaSuccess;
+  release();
+  return ok ? MUON_OK : MUON_ERR_CUDA;
+}
