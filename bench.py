@@ -474,12 +474,13 @@ def run_ours(args, w):
         h.copy_(d)
     h2d = sum(x.numel() * x.element_size() for x in (hW, hG, hM))
     d2h = sum(x.numel() * x.element_size() for x in (hW, hM))
-    # three staging buffers of about an eighth of the state each, at most 2 GB
-    part = max(plan.host_staging_bytes // 3, min(2 << 30, h2d // 8))
-    staging = torch.empty(3 * part + 256, dtype=torch.uint8, device=dev)
+    # args.host_bufs staging buffers of args.host_unit_gb each (at least one
+    # slice, at most an eighth of the state)
+    part = max(plan.host_unit_bytes, min(int(args.host_unit_gb * (1 << 30)), h2d // 8))
+    staging = torch.empty(args.host_bufs * part, dtype=torch.uint8, device=dev)
     del W, G, M, step   # the device copies are not needed any more
     host_step = mu.PreparedHostStep(plan, Wh, Gh, Mh, workspace=wsp, staging=staging,
-                                    stream=stream, **hp)
+                                    unit_bytes=part, stream=stream, **hp)
 
     for _ in range(min(args.warmup, 3)):
         host_step()
@@ -561,7 +562,7 @@ def run_ours(args, w):
                       "mode": mode},
            "roofline": roof, "kernels": kernels,
            "e2e": {"value": weak_scaling_value(n_slices, ws_n, ms_e2e), "unit": UNIT,
-                   "ms_per_step": ms_e2e,
+                   "ms_per_step": ms_e2e, "unit_bytes": part, "buffers": args.host_bufs,
                    "call": "muon_step_host: parameters, gradients and momenta in page-locked "
                            "host memory; per step every unit of slices is copied in, stepped "
                            "and its parameters and momenta copied back, the copies of one unit "
@@ -587,6 +588,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dense_24L", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-unit-gb", type=float, default=2.0,
+                    help="end-to-end leg: staging bytes of one unit of slices (GiB)")
+    ap.add_argument("--host-bufs", type=int, default=4,
+                    help="end-to-end leg: staging buffers in rotation")
     ap.add_argument("--ns-steps", type=int, default=None,
                     help="Newton-Schulz steps T (default: the workload's, 5); T = 0 times "
                          "the step without the iteration, for its share of the step")

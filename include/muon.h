@@ -308,34 +308,38 @@ MUON_API muon_status muon_step_timed(const muon_plan_t* plan, void* const* param
 /*
  * muon_step on parameters, gradients and momenta held in HOST memory (an
  * optimizer whose state lives in host memory; on a Grace-Blackwell node the
- * GPU reaches it over NVLink-C2C).  The plan's slices are cut into units of
- * whole slices that fit a third of `staging`; each unit's parameters,
- * gradients and momenta are copied to the device, stepped by the kernels of
- * muon_step, and its parameters and momenta copied back, the copies of one
- * unit overlapping the kernels of its neighbours (three staging buffers in
- * rotation, two copy streams of the call's own).
+ * GPU reaches it over NVLink-C2C).  `staging` is cut into
+ * nbuf = staging_bytes / unit_bytes buffers (2 to 16) and the plan's slices
+ * into units of whole slices that fit one; each unit's parameters, gradients
+ * and momenta are copied to the device, stepped by the kernels of muon_step,
+ * and its parameters and momenta copied back, the copies of one unit
+ * overlapping the kernels of its neighbours (two copy streams of the call's
+ * own).  The kernels do not wait as long as a unit's copies in and out take
+ * at most about nbuf - 1 times as long as its kernels.
  *   params, grads, momentum  host pointers (page-locked memory gives full
  *                            copy bandwidth; pageable memory works, slower),
  *                            shapes and dtypes as for muon_step
  *   workspace, ws_bytes      device, as for muon_step
- *   staging, staging_bytes   device, 256-byte aligned, at least
- *                            muon_plan_host_staging_bytes; larger staging
- *                            gives larger units (fewer launches) and a longer
- *                            pipeline fill and drain
+ *   staging, staging_bytes   device, 256-byte aligned
+ *   unit_bytes               staging bytes of one unit, at least
+ *                            muon_plan_host_unit_bytes; larger units mean
+ *                            fewer launches and a longer pipeline fill and
+ *                            drain
  * Asynchronous: the work is ordered before any later work on `stream`;
  * synchronise `stream` before reading the host buffers.  Returns
- * MUON_ERR_WORKSPACE when one slice does not fit a third of the staging.
- * Other arguments are those of muon_step.  The RFC has no counterpart of
- * this call.
+ * MUON_ERR_WORKSPACE when one slice does not fit unit_bytes or the staging
+ * holds fewer than two units.  Other arguments are those of muon_step.  The
+ * RFC has no counterpart of this call.
  */
 MUON_API muon_status muon_step_host(const muon_plan_t* plan, void* const* params,
                                     const void* const* grads, float* const* momentum, float lr,
                                     float beta, float wd, int nesterov, int ns_steps,
                                     const float* coeffs, void* workspace, size_t ws_bytes,
-                                    void* staging, size_t staging_bytes, void* stream);
-/* smallest staging for muon_step_host: three copies of the largest slice's
- * parameter, gradient and momentum (host only, no device call) */
-MUON_API muon_status muon_plan_host_staging_bytes(const muon_plan_t* plan, size_t* out);
+                                    void* staging, size_t staging_bytes, size_t unit_bytes,
+                                    void* stream);
+/* smallest unit_bytes of muon_step_host: the largest slice's parameter,
+ * gradient and momentum, each 256-byte aligned (host only, no device call) */
+MUON_API muon_status muon_plan_host_unit_bytes(const muon_plan_t* plan, size_t* out);
 
 /* Kernel launches muon_step makes for this plan and ns_steps, for a step
  * without O outputs (for accounting; no device call). */

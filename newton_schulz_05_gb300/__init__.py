@@ -70,7 +70,7 @@ EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
            "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
            "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static",
            "muon_step_amp", "muon_adamw_step", "muon_plan_partition", "muon_static_error",
-           "muon_step_timed", "muon_step_host", "muon_plan_host_staging_bytes"]
+           "muon_step_timed", "muon_step_host", "muon_plan_host_unit_bytes"]
 
 STATIC_WORKSPACE_BYTES = 32 << 20   # MUON_STATIC_WORKSPACE_BYTES in include/muon.h
 
@@ -108,8 +108,8 @@ def load(path: str = LIB_PATH):
     L.muon_step.argtypes = step_args
     L.muon_step_ortho.argtypes = step_args + [PP]
     L.muon_step_timed.argtypes = step_args + [ctypes.POINTER(_KernelTimes)]
-    L.muon_step_host.argtypes = step_args[:12] + [vp, sz, vp]
-    L.muon_plan_host_staging_bytes.argtypes = [vp, ctypes.POINTER(sz)]
+    L.muon_step_host.argtypes = step_args[:12] + [vp, sz, sz, vp]
+    L.muon_plan_host_unit_bytes.argtypes = [vp, ctypes.POINTER(sz)]
     L.muon_step_static.argtypes = step_args[:10] + [vp]
     L.muon_step_amp.argtypes = step_args[:10] + [ctypes.c_float, vp, vp, sz, vp]
     L.muon_adamw_step.argtypes = [ctypes.c_int, PP, PP, PP, PP, ctypes.POINTER(ctypes.c_int64),
@@ -130,7 +130,7 @@ def load(path: str = LIB_PATH):
                "muon_step_ortho", "muon_workspace_error", "muon_plan_launches",
                "muon_step_static", "muon_step_amp", "muon_adamw_step", "muon_plan_partition",
                "muon_static_error", "muon_step_timed", "muon_step_host",
-               "muon_plan_host_staging_bytes"):
+               "muon_plan_host_unit_bytes"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -223,10 +223,10 @@ class Plan:
         return g.value, i.value
 
     @property
-    def host_staging_bytes(self) -> int:
-        """Smallest device staging buffer of muon_step_host for this plan."""
+    def host_unit_bytes(self) -> int:
+        """Smallest staging unit of muon_step_host for this plan."""
         v = ctypes.c_size_t()
-        _check(load().muon_plan_host_staging_bytes(self._h, ctypes.byref(v)), "host_staging_bytes")
+        _check(load().muon_plan_host_unit_bytes(self._h, ctypes.byref(v)), "host_unit_bytes")
         return v.value
 
     def launches(self, ns_steps: int = 5) -> int:
@@ -449,11 +449,13 @@ class PreparedHostStep:
     memory, streamed through a device staging buffer) with its argument
     arrays marshalled once.  params/grads/momentum: CPU tensors, contiguous
     (page-locked for full copy bandwidth); the call updates params and
-    momentum in place once the stream has run it."""
+    momentum in place once the stream has run it.  The staging is cut into
+    units of unit_bytes (default: a third of it)."""
 
     def __init__(self, plan: Plan, params, grads, momentum, *, lr: float, beta: float, wd: float,
                  nesterov: bool = True, ns_steps: int = 5, coeffs=DEFAULT_COEFFS,
-                 workspace: torch.Tensor, staging: torch.Tensor, stream=None):
+                 workspace: torch.Tensor, staging: torch.Tensor, unit_bytes: int = 0,
+                 stream=None):
         n = len(plan.shapes)
         if not (len(params) == len(grads) == len(momentum) == n):
             raise ValueError("expected %d params, grads and momentum tensors" % n)
@@ -476,6 +478,7 @@ class PreparedHostStep:
                       ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                       ctypes.c_void_p(staging.data_ptr()),
                       ctypes.c_size_t(staging.numel() * staging.element_size()),
+                      ctypes.c_size_t(unit_bytes or staging.numel() * staging.element_size() // 3),
                       ctypes.c_void_p(_stream_handle(stream))]
 
     def __call__(self) -> None:

@@ -3,19 +3,20 @@
 // (on a Grace-Blackwell node the GPU reaches it over NVLink-C2C); the step
 // then streams it through a device staging buffer.
 //
-// The plan's slices are cut into units that fit a third of the staging
-// buffer (whole slices of one group, at most a dense chunk or one fused
-// launch).  Unit k is copied in on its own stream, stepped on the caller's
-// stream and copied out on a third stream, in buffer third k % 3, so the
-// copies of one unit overlap the kernels of its neighbours:
+// The staging buffer is cut into nbuf = staging_bytes / unit_bytes buffers
+// and the plan's slices into units that fit one (whole slices of one group,
+// at most a dense chunk or one fused launch).  Unit k is copied in on its
+// own stream, stepped on the caller's stream and copied out on a third
+// stream, in buffer k % nbuf, so the copies of one unit overlap the kernels
+// of its neighbours:
 //
 //   h2d stream   [in 0][in 1]      [in 2]      [in 3] ...
 //   caller       .     [step 0]    [step 1]    [step 2] ...
 //   d2h stream   .     .           [out 0]     [out 1] ...
 //
-// Buffer k % 3 takes unit k + 3 once unit k has been copied out, so the
-// kernels never wait as long as a unit's copies in and out take together at
-// most about twice as long as its kernels.
+// Buffer k % nbuf takes unit k + nbuf once unit k has been copied out, so
+// the kernels never wait as long as a unit's copies in and out take together
+// at most about nbuf - 1 times as long as its kernels.
 //
 // A unit's parameters, gradients and momenta go in (2 + 2 + 4 bytes per bf16
 // element); its parameters and momenta come back (2 + 4).  Contiguous slices
@@ -31,7 +32,7 @@ using namespace muon;
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kBufs = 3;   // staging buffers in rotation
+constexpr int kMaxBufs = 16;   // staging buffers in rotation, at most
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Unit {
@@ -81,11 +82,11 @@ void add_run(std::vector<Copy>& v, void* dst, const void* src, size_t bytes, boo
 
 }  // namespace
 
-extern "C" muon_status muon_plan_host_staging_bytes(const muon_plan_t* P, size_t* out) {
+extern "C" muon_status muon_plan_host_unit_bytes(const muon_plan_t* P, size_t* out) {
   if (!P || !out) return MUON_ERR_INVALID_ARG;
   size_t m = 0;
   for (const Group& g : P->groups) m = std::max(m, slice_stage_bytes(g));
-  *out = kBufs * m;
+  *out = m;
   return MUON_OK;
 }
 
@@ -93,7 +94,8 @@ extern "C" muon_status muon_step_host(const muon_plan_t* P, void* const* params,
                                       const void* const* grads, float* const* momentum,
                                       float lr, float beta, float wd, int nesterov, int ns_steps,
                                       const float* coeffs, void* workspace, size_t ws_bytes,
-                                      void* staging, size_t staging_bytes, void* stream) {
+                                      void* staging, size_t staging_bytes, size_t unit_bytes,
+                                      void* stream) {
   if (!P) return MUON_ERR_INVALID_ARG;
   const int np = (int)P->shapes.size();
   if (np > 0 && (!params || !grads || !momentum)) return MUON_ERR_INVALID_ARG;
@@ -113,7 +115,10 @@ extern "C" muon_status muon_step_host(const muon_plan_t* P, void* const* params,
   st.c = coeffs ? coeffs[2] : 2.0315f;
   if (!std::isfinite(st.a) || !std::isfinite(st.b) || !std::isfinite(st.c)) return MUON_ERR_INVALID_ARG;
   st.eps = P->opt.eps;
-  const size_t part = (staging_bytes / kBufs) / kAlign * kAlign;
+  const size_t part = unit_bytes / kAlign * kAlign;
+  if (part == 0) return MUON_ERR_INVALID_ARG;
+  const int nbuf = (int)std::min<size_t>(staging_bytes / part, (size_t)kMaxBufs);
+  if (nbuf < 2) return MUON_ERR_WORKSPACE;
   std::vector<Unit> units;
   muon_status ms = make_units(P, part, units);
   if (ms != MUON_OK) return ms;
@@ -126,24 +131,25 @@ extern "C" muon_status muon_step_host(const muon_plan_t* P, void* const* params,
   char* ws = static_cast<char*>(workspace);
   int* err_word = reinterpret_cast<int*>(ws);
   char* body = ws + kHeaderBytes;
-  char* stage[kBufs];
-  for (int b = 0; b < kBufs; ++b) stage[b] = static_cast<char*>(staging) + (size_t)b * part;
+  char* stage[kMaxBufs];
+  for (int b = 0; b < nbuf; ++b) stage[b] = static_cast<char*>(staging) + (size_t)b * part;
 
   // copy streams and events of this call, released when their work is done
   cudaStream_t h2d = nullptr, d2h = nullptr;
-  cudaEvent_t entry = nullptr, in_done[kBufs] = {}, step_done[kBufs] = {}, out_done[kBufs] = {};
+  cudaEvent_t entry = nullptr, in_done[kMaxBufs] = {}, step_done[kMaxBufs] = {},
+              out_done[kMaxBufs] = {};
   auto release = [&]() {
     if (h2d) cudaStreamDestroy(h2d);
     if (d2h) cudaStreamDestroy(d2h);
     if (entry) cudaEventDestroy(entry);
-    for (int b = 0; b < kBufs; ++b)
+    for (int b = 0; b < nbuf; ++b)
       for (cudaEvent_t e : {in_done[b], step_done[b], out_done[b]})
         if (e) cudaEventDestroy(e);
   };
   bool ok = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&entry, cudaEventDisableTiming) == cudaSuccess;
-  for (int b = 0; b < kBufs && ok; ++b)
+  for (int b = 0; b < nbuf && ok; ++b)
     ok = cudaEventCreateWithFlags(&in_done[b], cudaEventDisableTiming) == cudaSuccess &&
          cudaEventCreateWithFlags(&step_done[b], cudaEventDisableTiming) == cudaSuccess &&
          cudaEventCreateWithFlags(&out_done[b], cudaEventDisableTiming) == cudaSuccess;
@@ -158,7 +164,7 @@ extern "C" muon_status muon_step_host(const muon_plan_t* P, void* const* params,
   for (size_t k = 0; k < units.size() && ok; ++k) {
     const Unit& u = units[k];
     const Group& g = P->groups[u.group];
-    const int b = (int)(k % kBufs);
+    const int b = (int)(k % nbuf);
     const size_t es = g.dtype == MUON_BF16 ? 2 : 4;
     const size_t mn = (size_t)g.M * (size_t)g.N;
     const int ns = u.i1 - u.i0;
@@ -215,7 +221,7 @@ extern "C" muon_status muon_step_host(const muon_plan_t* P, void* const* params,
     ok = ok && cudaEventRecord(out_done[b], d2h) == cudaSuccess;
   }
   // the caller's stream continues after every copy out
-  for (int b = 0; b < kBufs && ok; ++b) ok = cudaStreamWaitEvent(s, out_done[b], 0) == cudaSuccess;
+  for (int b = 0; b < nbuf && ok; ++b) ok = cudaStreamWaitEvent(s, out_done[b], 0) == cudaSuccess;
   release();
   return ok ? MUON_OK : MUON_ERR_CUDA;
 }
