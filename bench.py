@@ -485,6 +485,19 @@ def run_ours(args, w):
     for _ in range(min(args.warmup, 3)):
         host_step()
     torch.cuda.synchronize(dev)
+    # the plain copy bandwidth of this host memory right now, for reference:
+    # one copy in of the gradients and one copy out into them
+    probe = torch.empty(hG.numel(), dtype=hG.dtype, device=dev)
+    c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    c0.record(stream)
+    probe.copy_(hG, non_blocking=True)
+    c1.record(stream)
+    hG.copy_(probe, non_blocking=True)
+    c2.record(stream)
+    torch.cuda.synchronize(dev)
+    gb = hG.numel() * hG.element_size() / 1e9
+    copy_gbs = {"h2d": gb / (c0.elapsed_time(c1) * 1e-3), "d2h": gb / (c1.elapsed_time(c2) * 1e-3)}
+    del probe
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_steps = max(1, min(args.steps, 50))
     e0.record(stream)
@@ -563,6 +576,7 @@ def run_ours(args, w):
            "roofline": roof, "kernels": kernels,
            "e2e": {"value": weak_scaling_value(n_slices, ws_n, ms_e2e), "unit": UNIT,
                    "ms_per_step": ms_e2e, "unit_bytes": part, "buffers": args.host_bufs,
+                   "plain_copy_GBps": copy_gbs,
                    "call": "muon_step_host: parameters, gradients and momenta in page-locked "
                            "host memory; per step every unit of slices is copied in, stepped "
                            "and its parameters and momenta copied back, the copies of one unit "
