@@ -60,9 +60,10 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float* v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-// vec: 1 when every slice's rows start 16-byte aligned for the fp32
-// momentum (n % 4 == 0, aligned bases); 2 (bf16 only) when moreover the
-// gradient rows are 16-byte aligned (n % 8 == 0): 8 elements per thread
+// vec: every slice's rows start 16-byte aligned (n % 4 == 0, aligned
+// bases): 4 consecutive elements per thread, 8-byte bf16 gradient loads (16-
+// byte loads of 8 elements per thread measured slower on the dense set:
+// 12.5 against 11.2 ms per step)
 template <typename PT>
 __global__ void __launch_bounds__(kNT) front_kernel(
     const __grid_constant__ SlicePtrs ptrs, int64_t m, int64_t n, int64_t m_pad,
@@ -85,44 +86,6 @@ __global__ void __launch_bounds__(kNT) front_kernel(
   __shared__ float tile[kFrontTileC][kFrontTileR + 1];
   float ss = 0.f;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if constexpr (sizeof(PT) == 2) {
-    if (!tr && vec == 2) {
-      // working (i, k) = stored (i, k); 8 consecutive elements per thread
-      // (one 16-byte gradient load), half a warp per 128-column row
-      for (int r = 2 * warp + (lane >> 4); r < kFrontTileR; r += kNT / 16) {
-        const int64_t i = i0 + r;
-        const int64_t k = k0 + 8 * (lane & 15);
-        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (i < m && k < n) {   // n is a multiple of 8: all 8 columns are in
-          const int64_t idx = i * n + k;
-          const uint4 gu = *reinterpret_cast<const uint4*>(G + idx);
-          const float4 ma = *reinterpret_cast<const float4*>(Mo + idx);
-          const float4 mb = *reinterpret_cast<const float4*>(Mo + idx + 4);
-          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gu);
-          float g[8], mo[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-          #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(g2[e]);
-            g[2 * e] = f.x; g[2 * e + 1] = f.y;
-          }
-          #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            g[e] *= gscale;
-            mo[e] = fmaf(beta, mo[e], g[e]);
-            v[e] = nesterov ? fmaf(beta, mo[e], g[e]) : mo[e];
-            ss = fmaf(v[e], v[e], ss);
-          }
-          *reinterpret_cast<float4*>(Mo + idx) = make_float4(mo[0], mo[1], mo[2], mo[3]);
-          *reinterpret_cast<float4*>(Mo + idx + 4) = make_float4(mo[4], mo[5], mo[6], mo[7]);
-        }
-        *reinterpret_cast<float4*>(V + i * n_pad + k) = make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4*>(V + i * n_pad + k + 4) = make_float4(v[4], v[5], v[6], v[7]);
-      }
-      const float tot = block_sum<kNT>(ss, red);
-      if (threadIdx.x == 0) part[blockIdx.x] = tot;
-      return;
-    }
-  }
   if (!tr && vec) {
     // working (i, k) = stored (i, k); 4 consecutive elements per thread
     for (int r = warp; r < kFrontTileR; r += kNT / 32) {
@@ -327,13 +290,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
     if (a % (4 * es) || reinterpret_cast<uintptr_t>(ptrs.Mom[i]) % 16) vec = 0;
     if (ptrs.O[i] && reinterpret_cast<uintptr_t>(ptrs.O[i]) % 16) vec = 0;
   }
-  // 16-byte gradient loads in the front kernel (bf16, rows of 8 elements)
-  int vec_front = vec;
-  if (vec && g.dtype == MUON_BF16 && g.n % 8 == 0 && !g.tr) {
-    vec_front = 2;
-    for (int i = 0; i < ns; ++i)
-      if (reinterpret_cast<uintptr_t>(ptrs.G[i]) % 16) vec_front = 1;
-  }
+
   // every launch after the step's first may overlap the previous kernel's
   // tail (programmatic dependent launch; each kernel waits before reading)
   cudaError_t le;
@@ -342,7 +299,7 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
     st.mark(MUON_KC_FRONT);
     if (g.dtype == MUON_BF16)
       le = launch_k(front_kernel<__nv_bfloat16>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m,
-                    g.n, mp, np, (int)g.tr, vec_front, st.beta, st.nesterov, st.gscale, st.skip,
+                    g.n, mp, np, (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip,
                     (const int*)err_word, ws, sws, off.V, off.part);
     else
       le = launch_k(front_kernel<float>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m, g.n, mp,
