@@ -169,31 +169,40 @@ class ClockSampler:
                 "sm_max_mhz": num(rows[0][2]), "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def source_digest(path: str) -> str:
-    """sha256 of a C/C++/CUDA source with its comments and blank space
-    removed, so that an edit of comments alone keeps a profile valid while
-    any change of code invalidates it."""
+def _code_text(path: str) -> str:
     import re
     text = open(path).read()
     text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
     text = re.sub(r"//[^\n]*", " ", text)
-    text = " ".join(text.split())
-    return hashlib.sha256(text.encode()).hexdigest()
+    return " ".join(text.split())
 
 
-def profile_value(profile: str, source: str, key: str):
+def source_digest(path: str) -> str:
+    """sha256 of a C/C++/CUDA source with its comments and blank space
+    removed, so that an edit of comments alone keeps a profile valid while
+    any change of code invalidates it."""
+    return hashlib.sha256(_code_text(path).encode()).hexdigest()
+
+
+def sources_digest(names) -> str:
+    """source_digest over several sources of the library (csrc/ names)."""
+    texts = [_code_text(os.path.join(ROOT, "newton_schulz_05_gb300", "csrc", n)) for n in names]
+    return hashlib.sha256("\n".join(texts).encode()).hexdigest()
+
+
+def profile_value(profile: str, sources, key: str):
     """A number from a committed ncu summary, valid only while the kernel
-    source it was captured from is unchanged (by source_digest)."""
+    sources it was captured from are unchanged (by their digest)."""
     path = os.path.join(ROOT, "profiles", profile)
-    src = os.path.join(ROOT, "newton_schulz_05_gb300", "csrc", source)
     if not os.path.exists(path):
         return None
+    names = [sources] if isinstance(sources, str) else list(sources)
     kv = {}
     for line in open(path):
         if ":" in line:
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("source digest") != source_digest(src) or key not in kv:
+    if kv.get("source digest") != sources_digest(names) or key not in kv:
         return None
     return float(kv[key].split()[0])
 
@@ -539,9 +548,13 @@ def run_ours(args, w):
         g_n = kernels.get("gemm", {}).get("launches_per_step", 0)
         achieved = dense_sym / (g_ms * 1e-3) / 1e12 if g_ms > 0 else 0.0
         step_achieved = flops_sym / (ms * 1e-3) / 1e12
+        traffic = None
+        if w.name == "dense_24L":
+            traffic = profile_value("tc_gemm_traffic_dense.txt", ["tc_gemm.cu", "dense.cu"],
+                                    "dram bytes per launch (dense_24L, scaled)")
         roof = {"bound": "tensor", "kernel": "tc_gemm (Newton-Schulz products)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None,
+                "traffic": traffic,
                 "launch_ms": g_ms / g_n if g_n else None,
                 "flops_per_launch": dense_sym / g_n if g_n else None,
                 "achieved_standard_count": dense_std / (g_ms * 1e-3) / 1e12 if g_ms > 0 else 0.0,

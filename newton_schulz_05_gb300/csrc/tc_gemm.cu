@@ -282,13 +282,17 @@ __device__ __forceinline__ void tm_ld32(uint32_t taddr, float* v) {
 }
 
 // tile index -> (batch, row tile I, col tile J); symmetric outputs only
-// enumerate tiles whose second 128-column half reaches the diagonal
+// enumerate tiles whose second 128-column half reaches the diagonal.  Other
+// products run down the columns (row tile fastest): the CTAs in flight then
+// share a few column panels of B, read from DRAM once, and sweep the rows of
+// A, which stay in L2 (for X' = B' X with X of [4096, 11008] the row-major
+// order re-read X about eight times per slice)
 __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& b, int& I, int& J) {
   b = t / p.tiles_per_batch;
   int r = t % p.tiles_per_batch;
   if (!p.sym) {
-    I = r / p.tiles_n;
-    J = r % p.tiles_n;
+    I = r % p.tiles_m;
+    J = r / p.tiles_m;
     return;
   }
   for (I = 0; I < p.tiles_m; ++I) {
@@ -604,13 +608,14 @@ __device__ __forceinline__ void mma2_commit_local(uint64_t* bar) {
 }
 
 // pair tile index -> (batch, 256-row tile I2, 256-column tile J); symmetric
-// outputs enumerate the tiles with J >= I2
+// outputs enumerate the tiles with J >= I2, other products run down the
+// columns (as tile_coords)
 __device__ __forceinline__ void pair_tile_coords(const TcParams& p, int t, int& b, int& I2, int& J) {
   b = t / p.tiles_per_batch;
   int r = t % p.tiles_per_batch;
   if (!p.sym) {
-    I2 = r / p.tiles_n;
-    J = r % p.tiles_n;
+    I2 = r % p.tiles_m;
+    J = r / p.tiles_m;
     return;
   }
   for (I2 = 0; I2 < p.tiles_n; ++I2) {
