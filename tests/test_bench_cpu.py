@@ -75,3 +75,17 @@ def test_profile_value_needs_a_matching_digest(tmp_path, monkeypatch):
     assert bench.profile_value("k.txt", "k.cu", "dram bytes per launch") == 1234.0
     (src / "k.cu").write_text("__global__ void k() { int x = 0; }\n")
     assert bench.profile_value("k.txt", "k.cu", "dram bytes per launch") is None
+
+
+@pytest.mark.parametrize("clocks,rejected", [
+    ({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 10}, False),
+    ({"sm_mhz": 1490.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 10}, False),
+    ({"sm_mhz": 1900.0, "sm_max_mhz": 2070.0, "reasons": ["hw_slowdown"], "samples": 10}, True),
+    ({"sm_mhz": 1900.0, "sm_max_mhz": 2070.0, "reasons": ["sw_thermal_slowdown"], "samples": 5}, True),
+    ({"sm_mhz": 1000.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 10}, True),
+    ({"sm_mhz": 1000.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 2}, False),
+    ({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}, False),
+])
+def test_clock_record_rejection_rule(clocks, rejected):
+    # without a process group the decision is this rank's own
+    assert bench.clock_rejected(clocks, torch.device("cpu")) is rejected
