@@ -489,20 +489,20 @@ def run_ours(args, w):
     # muon_step_host call per step, which copies each unit of slices in,
     # steps it and copies its parameters and momenta back, copies
     # overlapping the kernels.  Each kind of state lives in one flat host
-    # buffer, the parameters being views into it (the layout of a
-    # flat-parameter data-parallel trainer).
-    def flat(ts, device, pin=False):
-        buf = torch.empty(sum(x.numel() for x in ts), dtype=ts[0].dtype, device=device,
-                          pin_memory=pin)
+    # buffer from muon_host_alloc (page-locked, on transparent huge pages),
+    # the parameters being views into it (the layout of a flat-parameter
+    # data-parallel trainer).
+    def flat(ts):
+        buf = mu.alloc_host(sum(x.numel() for x in ts), ts[0].dtype)
         views, off = [], 0
         for x in ts:
             views.append(buf[off:off + x.numel()].view(x.shape))
             off += x.numel()
         return buf, views
 
-    hW, Wh = flat(W, "cpu", True)
-    hG, Gh = flat(G, "cpu", True)
-    hM, Mh = flat(M, "cpu", True)
+    hW, Wh = flat(W)
+    hG, Gh = flat(G)
+    hM, Mh = flat(M)
     for d, h in zip(W + G + M, Wh + Gh + Mh):
         h.copy_(d)
     h2d = sum(x.numel() * x.element_size() for x in (hW, hG, hM))
@@ -615,7 +615,8 @@ def run_ours(args, w):
                    "ms_per_step": ms_e2e, "unit_bytes": part, "buffers": args.host_bufs,
                    "plain_copy_GBps": copy_gbs,
                    "call": "muon_step_host: parameters, gradients and momenta in page-locked "
-                           "host memory; per step every unit of slices is copied in, stepped "
+                           "host memory from muon_host_alloc (transparent huge pages); per "
+                           "step every unit of slices is copied in, stepped "
                            "and its parameters and momenta copied back, the copies of one unit "
                            "overlapping the kernels of its neighbours",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -317,8 +317,9 @@ MUON_API muon_status muon_step_timed(const muon_plan_t* plan, void* const* param
  * own).  The kernels do not wait as long as a unit's copies in and out take
  * at most about nbuf - 1 times as long as its kernels.
  *   params, grads, momentum  host pointers (page-locked memory gives full
- *                            copy bandwidth; pageable memory works, slower),
- *                            shapes and dtypes as for muon_step
+ *                            copy bandwidth, and muon_host_alloc's keeps it
+ *                            when the state is cold; pageable memory works,
+ *                            slower), shapes and dtypes as for muon_step
  *   workspace, ws_bytes      device, as for muon_step
  *   staging, staging_bytes   device, 256-byte aligned
  *   unit_bytes               staging bytes of one unit, at least
@@ -340,6 +341,28 @@ MUON_API muon_status muon_step_host(const muon_plan_t* plan, void* const* params
 /* smallest unit_bytes of muon_step_host: the largest slice's parameter,
  * gradient and momentum, each 256-byte aligned (host only, no device call) */
 MUON_API muon_status muon_plan_host_unit_bytes(const muon_plan_t* plan, size_t* out);
+
+/*
+ * Page-locked host memory for the state muon_step_host streams: `bytes`
+ * rounded up to the kernel's transparent-huge-page size (the PMD size, read
+ * from sysfs; 2 MiB if it cannot be read), mapped at an address aligned to
+ * it, advised for huge pages, faulted in and registered with the CUDA driver
+ * (portable).  Huge pages keep the device's reads of state it has not touched
+ * for a while at full speed; with the base pages of the ordinary allocators,
+ * such cold reads ran at a fraction of the link's bandwidth on some
+ * allocations.  Where the kernel has no transparent huge pages the memory is
+ * still page-locked, on base pages.  *out (host) receives the address (NULL
+ * on failure); the memory reads as zeros.  Returns MUON_ERR_INVALID_ARG for
+ * bytes == 0 or out == NULL, MUON_ERR_NOMEM when the mapping fails (or under
+ * MUON_FAULT=alloc), MUON_ERR_CUDA when the registration fails (no device,
+ * or the driver refuses); nothing is held then.  Ownership: the caller's,
+ * until muon_host_free.
+ */
+MUON_API muon_status muon_host_alloc(size_t bytes, void** out);
+/* Unregisters and unmaps memory from muon_host_alloc.  NULL is a no-op;
+ * MUON_ERR_INVALID_ARG for an address muon_host_alloc did not return (or
+ * already freed).  No device work may still use the memory. */
+MUON_API muon_status muon_host_free(void* p);
 
 /* Kernel launches muon_step makes for this plan and ns_steps, for a step
  * without O outputs (for accounting; no device call). */

@@ -70,7 +70,8 @@ EXPORTS = ["muon_options_default", "muon_plan", "muon_plan_workspace_bytes",
            "muon_plan_slice", "muon_step", "muon_step_ortho", "muon_workspace_error",
            "muon_plan_launches", "muon_plan_destroy", "muon_status_string", "muon_step_static",
            "muon_step_amp", "muon_adamw_step", "muon_plan_partition", "muon_static_error",
-           "muon_step_timed", "muon_step_host", "muon_plan_host_unit_bytes"]
+           "muon_step_timed", "muon_step_host", "muon_plan_host_unit_bytes",
+           "muon_host_alloc", "muon_host_free"]
 
 STATIC_WORKSPACE_BYTES = 32 << 20   # MUON_STATIC_WORKSPACE_BYTES in include/muon.h
 
@@ -110,6 +111,8 @@ def load(path: str = LIB_PATH):
     L.muon_step_timed.argtypes = step_args + [ctypes.POINTER(_KernelTimes)]
     L.muon_step_host.argtypes = step_args[:12] + [vp, sz, sz, vp]
     L.muon_plan_host_unit_bytes.argtypes = [vp, ctypes.POINTER(sz)]
+    L.muon_host_alloc.argtypes = [sz, PP]
+    L.muon_host_free.argtypes = [vp]
     L.muon_step_static.argtypes = step_args[:10] + [vp]
     L.muon_step_amp.argtypes = step_args[:10] + [ctypes.c_float, vp, vp, sz, vp]
     L.muon_adamw_step.argtypes = [ctypes.c_int, PP, PP, PP, PP, ctypes.POINTER(ctypes.c_int64),
@@ -130,7 +133,7 @@ def load(path: str = LIB_PATH):
                "muon_step_ortho", "muon_workspace_error", "muon_plan_launches",
                "muon_step_static", "muon_step_amp", "muon_adamw_step", "muon_plan_partition",
                "muon_static_error", "muon_step_timed", "muon_step_host",
-               "muon_plan_host_unit_bytes"):
+               "muon_plan_host_unit_bytes", "muon_host_alloc", "muon_host_free"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -366,6 +369,27 @@ def workspace_error(workspace: torch.Tensor, stream=None, clear: bool = True) ->
     return code.value
 
 
+def _host_free(addr: int) -> None:
+    load().muon_host_free(ctypes.c_void_p(addr))
+
+
+def alloc_host(numel: int, dtype: torch.dtype) -> torch.Tensor:
+    """A CPU tensor of `numel` elements in page-locked, huge-page-backed host
+    memory from muon_host_alloc, for the state muon_step_host streams (zeros).
+    The memory is released by muon_host_free once the tensor and every view
+    of it are gone."""
+    import weakref
+    es = torch.empty(0, dtype=dtype).element_size()
+    nbytes = int(numel) * es
+    if nbytes <= 0:
+        raise ValueError("alloc_host needs at least one element")
+    p = ctypes.c_void_p()
+    _check(load().muon_host_alloc(ctypes.c_size_t(nbytes), ctypes.byref(p)), "muon_host_alloc")
+    buf = (ctypes.c_uint8 * nbytes).from_address(p.value)
+    weakref.finalize(buf, _host_free, p.value)   # runs when the last tensor view dies
+    return torch.frombuffer(buf, dtype=torch.uint8).view(dtype)
+
+
 def alloc_workspace(plan: Plan, device=None) -> torch.Tensor:
     """A zeroed device workspace of the plan's size (torch's allocator returns
     256-byte aligned blocks)."""
@@ -448,7 +472,8 @@ class PreparedHostStep:
     """A muon_step_host call (parameters, gradients and momenta in host
     memory, streamed through a device staging buffer) with its argument
     arrays marshalled once.  params/grads/momentum: CPU tensors, contiguous
-    (page-locked for full copy bandwidth); the call updates params and
+    (page-locked for full copy bandwidth: alloc_host gives memory that keeps
+    it when the state is cold); the call updates params and
     momentum in place once the stream has run it.  The staging is cut into
     units of unit_bytes (default: a third of it)."""
 

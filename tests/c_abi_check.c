@@ -99,6 +99,29 @@ int main(void) {
   }
   unsetenv("MUON_FAULT");
 
+  /* host-state allocator: argument checks, the fault switch, frees of NULL
+     and of an address it did not return.  With no device the registration
+     fails and nothing is held; with one, the memory is aligned and zeroed. */
+  {
+    void* hp = (void*)(uintptr_t)1;
+    CHECK(muon_host_alloc(0, &hp) == MUON_ERR_INVALID_ARG && hp == NULL);
+    CHECK(muon_host_alloc(4096, NULL) == MUON_ERR_INVALID_ARG);
+    CHECK(muon_host_free(NULL) == MUON_OK);
+    CHECK(muon_host_free((void*)(uintptr_t)0x123000) == MUON_ERR_INVALID_ARG);
+    setenv("MUON_FAULT", "alloc", 1);
+    hp = (void*)(uintptr_t)1;
+    CHECK(muon_host_alloc(4096, &hp) == MUON_ERR_NOMEM && hp == NULL);
+    unsetenv("MUON_FAULT");
+    muon_status hs = muon_host_alloc(4096, &hp);
+    if (hs == MUON_OK) {
+      CHECK(hp != NULL && (uintptr_t)hp % 4096 == 0 && ((unsigned char*)hp)[4095] == 0);
+      CHECK(muon_host_free(hp) == MUON_OK);
+      CHECK(muon_host_free(hp) == MUON_ERR_INVALID_ARG);
+    } else {
+      CHECK(hs == MUON_ERR_CUDA && hp == NULL);
+    }
+  }
+
   /* replicas: every slice has one owner, the loads sum up */
   int owner[78];
   double load[4];
