@@ -547,9 +547,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // only CTA 1 issued with CTA 1's bytes, and completing, for stages only CTA
 // 0 issued, the bytes CTA 1 never sent) and arrives on CTA 1's `drained`.
 // No CTA leaves with a copy in flight.
-constexpr int PSTAGES = 6;
-constexpr int B_HALF = 128 * BK * 2;               // 16 KB: this CTA's half of B
-constexpr int PSTAGE_BYTES = A_BYTES + B_HALF;     // 32 KB
+// A stage of the pair kernel spans PBOX 64-wide TMA boxes of K per operand
+// (a 128-byte-swizzled box row holds 64 fp16), so that one barrier wait and
+// one commit serve 4 * PBOX MMAs: with one box per stage that per-stage
+// work held the tensor pipe's math to 77% of its busy time.  A box of the
+// last stage that starts past the end of K is filled with zeros by TMA and
+// its MMAs are not issued.
+constexpr int PBOX = 2;                            // 64-wide K boxes per stage
+constexpr int PBK = PBOX * BK;                     // K per stage
+constexpr int PSTAGES = 3;
+constexpr int PSUB = 128 * BK * 2;                 // 16 KB: one 64-wide box of A, or of this CTA's B half
+constexpr int PA_BYTES = PBOX * PSUB;              // A of one stage
+constexpr int PSTAGE_BYTES = 2 * PBOX * PSUB;      // A and this CTA's half of B
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -673,7 +682,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   cluster_sync_all();   // barriers of both CTAs initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int kblocks = p.K / BK;
+  const int kblocks = (p.K + PBK - 1) / PBK;
   pdl_wait();
   // CTA 0 decides for the pair whether the step is skipped (a skipped
   // loss-scaled step, or a wait of the step that gave up), so that both
@@ -709,28 +718,34 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t ph = (it / PSTAGES) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, p.wait_limit)) { fail(); ok = false; break; }
           unsigned char* sa = smem + s * PSTAGE_BYTES;
-          unsigned char* sb = sa + A_BYTES;
+          unsigned char* sb = sa + PA_BYTES;
           const int row = I2 * 256 + (int)rank * 128;
           const int col = J * 256 + (int)rank * 128;
-          if (rank == 0) {
-            mbar_expect_tx(&loaded[s], 2 * PSTAGE_BYTES);   // both halves
-            tma_load_3d(sa, &tmA, &loaded[s], kb * BK, row, b);
-            if (!p.b_mn) {
-              tma_load_3d(sb, &tmB, &loaded[s], kb * BK, col, b);
+          if (rank == 0) mbar_expect_tx(&loaded[s], 2 * PSTAGE_BYTES);   // both halves
+          const uint32_t bar0 = mapa(smem_u32(&loaded[s]), 0);
+          #pragma unroll
+          for (int h = 0; h < PBOX; ++h) {
+            const int k0 = kb * PBK + h * BK;
+            unsigned char* ha = sa + h * PSUB;
+            unsigned char* hb = sb + h * PSUB;
+            if (rank == 0) {
+              tma_load_3d(ha, &tmA, &loaded[s], k0, row, b);
+              if (!p.b_mn) {
+                tma_load_3d(hb, &tmB, &loaded[s], k0, col, b);
+              } else {
+                #pragma unroll
+                for (int q = 0; q < 2; ++q)
+                  tma_load_3d(hb + q * (64 * BK * 2), &tmB, &loaded[s], col + q * 64, k0, b);
+              }
             } else {
-              #pragma unroll
-              for (int q = 0; q < 2; ++q)
-                tma_load_3d(sb + q * (64 * BK * 2), &tmB, &loaded[s], col + q * 64, kb * BK, b);
-            }
-          } else {
-            const uint32_t bar0 = mapa(smem_u32(&loaded[s]), 0);
-            tma_load_3d_pair(sa, &tmA, bar0, kb * BK, row, b);
-            if (!p.b_mn) {
-              tma_load_3d_pair(sb, &tmB, bar0, kb * BK, col, b);
-            } else {
-              #pragma unroll
-              for (int q = 0; q < 2; ++q)
-                tma_load_3d_pair(sb + q * (64 * BK * 2), &tmB, bar0, col + q * 64, kb * BK, b);
+              tma_load_3d_pair(ha, &tmA, bar0, k0, row, b);
+              if (!p.b_mn) {
+                tma_load_3d_pair(hb, &tmB, bar0, k0, col, b);
+              } else {
+                #pragma unroll
+                for (int q = 0; q < 2; ++q)
+                  tma_load_3d_pair(hb + q * (64 * BK * 2), &tmB, bar0, col + q * 64, k0, b);
+              }
             }
           }
         }
@@ -778,12 +793,15 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           if (!mbar_wait(&loaded[s], ph, p.wait_limit)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * PSTAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sb = sa + PA_BYTES;
           #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = sdesc(sa + k * 32, 16, 1024);
-            const uint64_t bd = p.b_mn ? sdesc(sb + k * 2048, 64 * BK * 2, 1024)
-                                       : sdesc(sb + k * 32, 16, 1024);
+          for (int k = 0; k < PBK / 16; ++k) {
+            if (PBOX > 1 && kb * PBK + (k / (BK / 16)) * BK >= p.K) break;   // zero-filled box
+            const uint32_t h = (uint32_t)(k / (BK / 16)) * PSUB;   // box of this K step
+            const int kk = k % (BK / 16);
+            const uint64_t ad = sdesc(sa + h + kk * 32, 16, 1024);
+            const uint64_t bd = p.b_mn ? sdesc(sb + h + kk * 2048, 64 * BK * 2, 1024)
+                                       : sdesc(sb + h + kk * 32, 16, 1024);
             mma2_f16(dt, ad, bd, p.idesc, (kb | k) != 0);
           }
           mma2_commit_both(&empty[s]);
