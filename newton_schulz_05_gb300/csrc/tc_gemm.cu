@@ -550,9 +550,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // A stage of the pair kernel spans PBOX 64-wide TMA boxes of K per operand
 // (a 128-byte-swizzled box row holds 64 fp16), so that one barrier wait and
 // one commit serve 4 * PBOX MMAs: with one box per stage that per-stage
-// work held the tensor pipe's math to 77% of its busy time.  A box of the
-// last stage that starts past the end of K is filled with zeros by TMA and
-// its MMAs are not issued.
+// work held the tensor pipe's math to 77% of its busy time.  K is a
+// multiple of PBK (the dense working dims are padded to 128); other
+// products take the one-CTA kernel.
 constexpr int PBOX = 2;                            // 64-wide K boxes per stage
 constexpr int PBK = PBOX * BK;                     // K per stage
 constexpr int PSTAGES = 3;
@@ -682,7 +682,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   cluster_sync_all();   // barriers of both CTAs initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int kblocks = (p.K + PBK - 1) / PBK;
+  const int kblocks = p.K / PBK;
   pdl_wait();
   // CTA 0 decides for the pair whether the step is skipped (a skipped
   // loss-scaled step, or a wait of the step that gave up), so that both
@@ -796,7 +796,6 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sb = sa + PA_BYTES;
           #pragma unroll
           for (int k = 0; k < PBK / 16; ++k) {
-            if (PBOX > 1 && kb * PBK + (k / (BK / 16)) * BK >= p.K) break;   // zero-filled box
             const uint32_t h = (uint32_t)(k / (BK / 16)) * PSUB;   // box of this K step
             const int kk = k % (BK / 16);
             const uint64_t ad = sdesc(sa + h + kk * 32, 16, 1024);
@@ -903,10 +902,11 @@ uint32_t tc_idesc_f16(int m, int n, int b_mn) {
 
 size_t tc_gemm_smem_bytes() { return STAGES * STAGE_BYTES + 4 * EPI_BYTES + 1024 + 256; }
 
-// the pair kernel for products with at least one 256-row tile, unless
-// MUON_GEMM=single selects the one-CTA kernel (for comparisons)
+// the pair kernel for products with at least one 256-row tile and K a
+// multiple of its stage, unless MUON_GEMM=single selects the one-CTA kernel
+// (for comparisons)
 static bool use_pair_kernel(const TcGemm& g) {
-  if (g.M < 256) return false;
+  if (g.M < 256 || g.K % PBK) return false;
   const char* e = std::getenv("MUON_GEMM");
   return !(e && std::strcmp(e, "single") == 0);
 }
