@@ -168,7 +168,12 @@ MUON_API muon_status muon_plan_slice(const muon_plan_t* plan, int param, int sli
  *   momentum[p] device, fp32, same shape, updated in place
  *   coeffs      host, 3 floats (a, b, c); null = (3.4445, -4.7750, 2.0315)
  *   ns_steps    T >= 0
- *   workspace   device, 256-byte aligned, >= muon_plan_workspace_bytes
+ *   workspace   device, 256-byte aligned, >= muon_plan_workspace_bytes.
+ *               Any content is valid on entry.  Passing the same workspace
+ *               to the next step of the same plan keeps, per dense slice, the
+ *               power of two that scales its first iterate; when it still
+ *               fits, the step skips one pass over that slice.  The results
+ *               do not depend on it.
  * Parameter, gradient and momentum buffers must not overlap one another.
  */
 MUON_API muon_status muon_step(const muon_plan_t* plan, void* const* params,

@@ -9,6 +9,16 @@
 //   T x        A = X X^T;  B = b*A + c*A*A;  X <- a*X + B*X   (GEMMs)
 //   epilogue   W' = W*(1 - lr*wd) - lr*scale*O  in the parameter layout
 //
+// With fp16 iterates and T > 0 V makes no round trip through memory.  The
+// front writes the first iterate as X~ = fp16(V 2^-e) with a per-slice power
+// of two e predicted from the slice's previous step, and the first Gram and
+// update scale their products by f = 2^e / (||V|| + eps) (f^2 for the Gram),
+// so that X~ stands for X0 = f X~.  finalize computes the slice's
+// e = 8 floor(log2 ||V|| / 8) - 7, which keeps every |X~| below 2^15 and its
+// typical element far above fp16's subnormals; a second pass of the front
+// rewrites X~ from G and M' for the slices whose prediction missed.  The
+// result never depends on the prediction.
+//
 // (HyperParallel FSDP Muon RFC, mindspore hyper-parallel issue
 // "HyperParallel FSDP Muon优化器性能优化 RFC": section 1(1) momentum input,
 // sections 2/3 batched slices, section 6 decoupled weight decay.)
@@ -16,6 +26,7 @@
 // Working buffers are padded to multiples of 128 with zeros.  Zero rows and
 // columns stay exactly zero under the iteration (A, B and the update of a
 // zero row or column are zero), so padding changes no result.
+#include <cstddef>
 #include <cstdio>
 
 #include "common.cuh"
@@ -28,6 +39,16 @@ namespace muon {
 namespace {
 
 constexpr int kNT = 256;
+
+// per-slice scale slot of the dense path (in the slice's workspace)
+struct ScaleSlot {
+  float inv;    // 1 / (||V|| + eps)
+  float f;      // 2^e / (||V|| + eps): X0 = f X~
+  float f2;     // f^2, the first Gram's factor
+  int redo;     // the front's exponent was not e: X~ is rewritten
+  int e;        // exponent of X~ = fp16(V 2^-e)
+};
+constexpr int kExpMin = -100, kExpMax = 100;   // 2^-e stays a finite fp32
 
 struct DenseBufs {
   float* V;        // [m_pad, n_pad] fp32: front output, then O
@@ -64,21 +85,38 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float* v) {
 // bases): 4 consecutive elements per thread, 8-byte bf16 gradient loads (16-
 // byte loads of 8 elements per thread measured slower on the dense set:
 // 12.5 against 11.2 ms per step)
-template <typename PT>
+// OUT: kOutV writes V (fp32); kOutX writes X~ = fp16(V 2^-e) with the
+// exponent predicted in exps[]; kOutRedo, for the slices whose prediction
+// missed, recomputes V from G and M' (no momentum update, no partial sums)
+// and writes X~ with the exact exponent.
+enum { kOutV = 0, kOutX = 1, kOutRedo = 2 };
+
+template <typename PT, int OUT>
 __global__ void __launch_bounds__(kNT) front_kernel(
     const __grid_constant__ SlicePtrs ptrs, int64_t m, int64_t n, int64_t m_pad,
     int64_t n_pad, int tr, int vec, float beta, int nesterov, float gscale, const int* skip,
-    const int* err, char* ws, size_t slice_ws, size_t off_V, size_t off_part) {
+    const int* err, char* ws, size_t slice_ws, size_t off_V, size_t off_X, size_t off_part,
+    size_t off_slot, const int* exps) {
   pdl_wait();
   // skipped loss-scaled step, or an earlier wait of the step gave up:
   // momentum untouched
   if ((skip && *skip) || *err) return;
   const int s = blockIdx.y;
+  char* base = ws + (size_t)s * slice_ws;
+  int e = 0;
+  if (OUT == kOutRedo) {
+    const ScaleSlot* slot = reinterpret_cast<const ScaleSlot*>(base + off_slot);
+    if (!slot->redo) return;
+    e = slot->e;
+  } else if (OUT == kOutX) {
+    e = min(max(exps[s], kExpMin), kExpMax);
+  }
+  const float xs = ldexpf(1.f, -e);   // exact power of two
   const int tiles_c = (int)(n_pad / kFrontTileC);
   const int64_t i0 = (int64_t)(blockIdx.x / tiles_c) * kFrontTileR;
   const int64_t k0 = (int64_t)(blockIdx.x % tiles_c) * kFrontTileC;
-  char* base = ws + (size_t)s * slice_ws;
   float* V = reinterpret_cast<float*>(base + off_V);
+  __half* X = reinterpret_cast<__half*>(base + off_X);
   float* part = reinterpret_cast<float*>(base + off_part);
   const PT* G = static_cast<const PT*>(ptrs.G[s]);
   float* Mo = ptrs.Mom[s];
@@ -86,6 +124,21 @@ __global__ void __launch_bounds__(kNT) front_kernel(
   __shared__ float tile[kFrontTileC][kFrontTileR + 1];
   float ss = 0.f;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // V of one element from its gradient g (scaled) and stored momentum
+  // index; the momentum is updated in place unless this is the redo pass
+  auto step = [&](float g, int64_t idx) {
+    if (OUT == kOutRedo) {
+      const float mm = Mo[idx];
+      return nesterov ? fmaf(beta, mm, g) : mm;
+    }
+    const float mm = fmaf(beta, Mo[idx], g);
+    Mo[idx] = mm;
+    return nesterov ? fmaf(beta, mm, g) : mm;
+  };
+  auto put = [&](int64_t w, float v) {   // working-layout element w
+    if (OUT == kOutV) V[w] = v;
+    else X[w] = __float2half_rn(v * xs);
+  };
   if (!tr && vec) {
     // working (i, k) = stored (i, k); 4 consecutive elements per thread
     for (int r = warp; r < kFrontTileR; r += kNT / 32) {
@@ -99,15 +152,24 @@ __global__ void __launch_bounds__(kNT) front_kernel(
         const float4 mm4 = *reinterpret_cast<const float4*>(Mo + idx);
         mo[0] = mm4.x; mo[1] = mm4.y; mo[2] = mm4.z; mo[3] = mm4.w;
         #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          g[e] *= gscale;
-          mo[e] = fmaf(beta, mo[e], g[e]);
-          v[e] = nesterov ? fmaf(beta, mo[e], g[e]) : mo[e];
-          ss = fmaf(v[e], v[e], ss);
+        for (int q = 0; q < 4; ++q) {
+          g[q] *= gscale;
+          if (OUT != kOutRedo) mo[q] = fmaf(beta, mo[q], g[q]);
+          v[q] = nesterov ? fmaf(beta, mo[q], g[q]) : mo[q];
+          ss = fmaf(v[q], v[q], ss);
         }
-        *reinterpret_cast<float4*>(Mo + idx) = make_float4(mo[0], mo[1], mo[2], mo[3]);
+        if (OUT != kOutRedo)
+          *reinterpret_cast<float4*>(Mo + idx) = make_float4(mo[0], mo[1], mo[2], mo[3]);
       }
-      *reinterpret_cast<float4*>(V + i * n_pad + k) = make_float4(v[0], v[1], v[2], v[3]);
+      if (OUT == kOutV) {
+        *reinterpret_cast<float4*>(V + i * n_pad + k) = make_float4(v[0], v[1], v[2], v[3]);
+      } else {
+        __half2 a = __floats2half2_rn(v[0] * xs, v[1] * xs), b = __floats2half2_rn(v[2] * xs, v[3] * xs);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&a);
+        u.y = *reinterpret_cast<uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(X + i * n_pad + k) = u;
+      }
     }
   } else if (!tr) {
     // working (i, k) = stored (i, k); stored slice is [m, n]
@@ -118,13 +180,10 @@ __global__ void __launch_bounds__(kNT) front_kernel(
         float v = 0.f;
         if (i < m && k < n) {
           const int64_t idx = i * n + k;
-          const float g = to_f(G[idx]) * gscale;
-          const float mm = fmaf(beta, Mo[idx], g);
-          Mo[idx] = mm;
-          v = nesterov ? fmaf(beta, mm, g) : mm;
+          v = step(to_f(G[idx]) * gscale, idx);
         }
         ss = fmaf(v, v, ss);
-        V[i * n_pad + k] = v;
+        put(i * n_pad + k, v);
       }
     }
   } else {
@@ -135,25 +194,31 @@ __global__ void __launch_bounds__(kNT) front_kernel(
       float v = 0.f;
       if (i < m && k < n) {
         const int64_t idx = k * m + i;
-        const float g = to_f(G[idx]) * gscale;
-        const float mm = fmaf(beta, Mo[idx], g);
-        Mo[idx] = mm;
-        v = nesterov ? fmaf(beta, mm, g) : mm;
+        v = step(to_f(G[idx]) * gscale, idx);
       }
       ss = fmaf(v, v, ss);
       tile[c][lane] = v;
     }
     __syncthreads();
     for (int r = warp; r < kFrontTileR; r += kNT / 32)
-      for (int c = lane; c < kFrontTileC; c += 32) V[(i0 + r) * n_pad + k0 + c] = tile[c][r];
+      for (int c = lane; c < kFrontTileC; c += 32) put((i0 + r) * n_pad + k0 + c, tile[c][r]);
   }
+  if (OUT == kOutRedo) return;
   const float tot = block_sum<kNT>(ss, red);
   if (threadIdx.x == 0) part[blockIdx.x] = tot;
 }
 
+// ||V|| per slice from the front's partial sums; with exps (the fp16 first
+// iterate X~ = fp16(V 2^-e)) also the slice's exponent e = 8 floor(log2
+// ||V|| / 8) - 7, the factors f = 2^e / (||V|| + eps) and f^2, and whether
+// the front's predicted exponent missed; e is stored back as the next step's
+// prediction.  2^7 <= ||V|| 2^-e < 2^15 bounds every |X~| below fp16's
+// largest value, and a prediction misses only when ||V|| crosses one of the
+// 2^8-wide bins.
 __global__ void __launch_bounds__(kNT) finalize_kernel(char* ws, size_t slice_ws,
-                                                       size_t off_part, size_t off_inv,
-                                                       int nblk, float eps, const int* err) {
+                                                       size_t off_part, size_t off_slot,
+                                                       int nblk, float eps, int* exps,
+                                                       const int* err) {
   pdl_wait();
   if (*err) return;
   char* base = ws + (size_t)blockIdx.x * slice_ws;
@@ -162,7 +227,25 @@ __global__ void __launch_bounds__(kNT) finalize_kernel(char* ws, size_t slice_ws
   float ss = 0.f;
   for (int i = threadIdx.x; i < nblk; i += kNT) ss += part[i];
   const float tot = block_sum<kNT>(ss, red);
-  if (threadIdx.x == 0) *reinterpret_cast<float*>(base + off_inv) = 1.f / (sqrtf(tot) + eps);
+  if (threadIdx.x != 0) return;
+  ScaleSlot* slot = reinterpret_cast<ScaleSlot*>(base + off_slot);
+  const float nrm = sqrtf(tot);
+  slot->inv = 1.f / (nrm + eps);
+  if (!exps) return;
+  int e = 0;
+  if (nrm > 0.f && isfinite(nrm)) {
+    int ex;
+    frexpf(nrm, &ex);          // nrm = q 2^ex, q in [0.5, 1): floor(log2 nrm) = ex - 1
+    const int L = ex - 1;
+    const int q = L >= 0 ? L / 8 : -((-L + 7) / 8);   // floor(L / 8)
+    e = min(max(8 * q - 7, kExpMin), kExpMax);
+  }
+  const float f = ldexpf(1.f, e) / (nrm + eps);
+  slot->f = f;
+  slot->f2 = f * f;
+  slot->redo = exps[blockIdx.x] != e ? 1 : 0;
+  slot->e = e;
+  exps[blockIdx.x] = e;
 }
 
 // X0 = s*V in the iterate type; with T == 0 the scaled V is O itself.
@@ -276,7 +359,8 @@ Offsets dense_offsets(const Group& g, int mode) {
 
 template <typename IT>
 cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
-                      const StepArgs& st, char* ws, int* err_word, cudaStream_t s, bool pdl_first) {
+                      const StepArgs& st, char* ws, int* exps, int* err_word, cudaStream_t s,
+                      bool pdl_first) {
   const Offsets off = dense_offsets(g, mode);
   const size_t sws = g.slice_ws;
   const int64_t mp = g.m_pad, np = g.n_pad;
@@ -291,33 +375,46 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
     if (ptrs.O[i] && reinterpret_cast<uintptr_t>(ptrs.O[i]) % 16) vec = 0;
   }
 
+  // fp16 iterates and T > 0: the front writes the first iterate itself
+  // (X~ = fp16(V 2^-e), see the header), and a second front pass fixes the
+  // slices whose exponent was mispredicted; otherwise V, then X0 = s V
+  const bool spec = sizeof(IT) == 2 && st.T > 0;
+  auto front = [&](auto kern, bool pdl) {
+    return launch_k(kern, fgrid, dim3(kNT), 0, s, pdl, ptrs, g.m, g.n, mp, np, (int)g.tr, vec,
+                    st.beta, st.nesterov, st.gscale, st.skip, (const int*)err_word, ws, sws,
+                    off.V, off.X0, off.part, off.inv, (const int*)exps);
+  };
+  const bool bf = g.dtype == MUON_BF16;
   // every launch after the step's first may overlap the previous kernel's
   // tail (programmatic dependent launch; each kernel waits before reading)
   cudaError_t le;
   {
     NvtxRange r("muon::front_kernel");
     st.mark(MUON_KC_FRONT);
-    if (g.dtype == MUON_BF16)
-      le = launch_k(front_kernel<__nv_bfloat16>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m,
-                    g.n, mp, np, (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip,
-                    (const int*)err_word, ws, sws, off.V, off.part);
+    if (spec)
+      le = bf ? front(front_kernel<__nv_bfloat16, kOutX>, pdl_first)
+              : front(front_kernel<float, kOutX>, pdl_first);
     else
-      le = launch_k(front_kernel<float>, fgrid, dim3(kNT), 0, s, pdl_first, ptrs, g.m, g.n, mp,
-                    np, (int)g.tr, vec, st.beta, st.nesterov, st.gscale, st.skip,
-                    (const int*)err_word, ws, sws, off.V, off.part);
+      le = bf ? front(front_kernel<__nv_bfloat16, kOutV>, pdl_first)
+              : front(front_kernel<float, kOutV>, pdl_first);
   }
   if (le != cudaSuccess) return le;
   {
     NvtxRange r("muon::finalize_kernel");
     st.mark(MUON_KC_NORM);
     le = launch_k(finalize_kernel, dim3(ns), dim3(kNT), 0, s, true, ws, sws, off.part, off.inv,
-                  nblk, st.eps, (const int*)err_word);
+                  nblk, st.eps, spec ? exps : nullptr, (const int*)err_word);
   }
   if (le != cudaSuccess) return le;
-  const int64_t cnt = mp * np;
-  int nb = (int)((cnt / 4 + kNT - 1) / kNT);
-  if (nb > 1184) nb = 1184;
-  {
+  if (spec) {
+    NvtxRange r("muon::front_kernel redo");
+    st.mark(MUON_KC_NORM);
+    le = bf ? front(front_kernel<__nv_bfloat16, kOutRedo>, true)
+            : front(front_kernel<float, kOutRedo>, true);
+  } else {
+    const int64_t cnt = mp * np;
+    int nb = (int)((cnt / 4 + kNT - 1) / kNT);
+    if (nb > 1184) nb = 1184;
     NvtxRange r("muon::normalize_kernel");
     st.mark(MUON_KC_NORM);
     le = launch_k(normalize_kernel<IT>, dim3(nb, ns), dim3(kNT), 0, s, true, ws, sws, off.V,
@@ -361,6 +458,10 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
       } else {
         g1.D2 = ws + off.A2; g1.alpha2 = st.c; g1.diag2 = st.b;
       }
+      if (t == 0) {   // X0 = f X~: the products of X~ scale by f^2
+        g1.alpha_base = ws + off.inv + offsetof(ScaleSlot, f2);
+        g1.alpha_stride = sws;
+      }
       cudaError_t e;
       {
         NvtxRange r("muon::tc_gemm gram");
@@ -397,6 +498,10 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
       g3.M = mp; g3.N = np; g3.K = mp;
       g3.A = ws + off.B; g3.B = ws + xin; g3.b_mn = 1;
       g3.D = ws + (last ? off.V : xout); g3.d_f32 = last ? 1 : 0;
+      if (t == 0) {   // X' = B' X0 = f (B' X~)
+        g3.alpha_base = ws + off.inv + offsetof(ScaleSlot, f);
+        g3.alpha_stride = sws;
+      }
       if (last && fuse) {
         g3.W = ptrs.W;
         g3.w_f32 = g.dtype == MUON_F32 ? 1 : 0;
@@ -514,11 +619,11 @@ cudaError_t launch_check_finite(const Group& g, const SlicePtrs& ptrs, int nslic
 }
 
 cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& ptrs,
-                                     int nslices, const StepArgs& st, char* ws,
+                                     int nslices, const StepArgs& st, char* ws, int* exps,
                                      int* err_word, cudaStream_t s, bool pdl_first) {
   if (mode == MUON_MODE_FP32)
-    return run_dense<float>(g, mode, ptrs, nslices, st, ws, err_word, s, pdl_first);
-  return run_dense<__half>(g, mode, ptrs, nslices, st, ws, err_word, s, pdl_first);
+    return run_dense<float>(g, mode, ptrs, nslices, st, ws, exps, err_word, s, pdl_first);
+  return run_dense<__half>(g, mode, ptrs, nslices, st, ws, exps, err_word, s, pdl_first);
 }
 
 }  // namespace muon

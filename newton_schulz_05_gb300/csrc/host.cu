@@ -299,7 +299,9 @@ extern "C" muon_status muon_step_host(const muon_plan_t* P, void* const* params,
       if (g.kernel == MUON_KERNEL_SKINNY)
         e = launch_skinny(g, ptrs, ns, st, err_word, s);
       else
-        e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body, err_word, s, false);
+        e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body,
+                                     reinterpret_cast<int*>(ws + P->exp_off) + g.exp_base + u.i0,
+                                     err_word, s, false);
       ok = e == cudaSuccess;
     }
     ok = ok && cudaEventRecord(step_done[b], s) == cudaSuccess;

@@ -56,6 +56,7 @@ struct Group {
   int64_t m_pad = 0, n_pad = 0;
   int chunk = 0;           // slices per chunk
   size_t slice_ws = 0;     // workspace bytes per slice
+  int exp_base = -1;       // index of the group's first slice in the exponent region
 };
 
 }  // namespace muon
@@ -67,6 +68,7 @@ struct muon_plan_s {
   std::vector<muon::Group> groups;
   muon_options opt;
   size_t ws_bytes = 0;
+  size_t exp_off = 0;   // exponent region: one int per dense slice, after the body
 };
 
 namespace muon {
@@ -119,9 +121,10 @@ cudaError_t launch_skinny(const Group& g, const SlicePtrs& ptrs, int nslices,
                           const StepArgs& st, int* err_word, cudaStream_t s);
 
 // pdl_first: the chunk's first kernel may overlap the previous kernel on the
-// stream (false for the first launch of a step)
+// stream (false for the first launch of a step).  exps: the exponent slots of
+// the chunk's slices (device, kept across calls; any content is valid)
 cudaError_t launch_dense_group_chunk(const Group& g, int mode, const SlicePtrs& ptrs,
-                                     int nslices, const StepArgs& st, char* ws,
+                                     int nslices, const StepArgs& st, char* ws, int* exps,
                                      int* err_word, cudaStream_t s, bool pdl_first);
 
 int dense_launches(int ns_steps, int mode, int tr);   // per chunk, step without O outputs

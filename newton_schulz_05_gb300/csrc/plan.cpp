@@ -151,20 +151,29 @@ muon_status muon_plan(const muon_shape* shapes, int n, const muon_options* opt,
       G.slice_e.push_back(e);
     }
   }
-  size_t ws = 0;
+  // dense groups: one exponent slot per slice, kept across calls in a
+  // region after the body (the scale of each slice's first iterate)
+  size_t nexp = 0;
   for (Group& G : P->groups) {
     if (configure_skinny(G, o)) {
       G.kernel = MUON_KERNEL_SKINNY;
       continue;
     }
     G.kernel = MUON_KERNEL_DENSE;
+    G.exp_base = (int)nexp;
+    nexp += (size_t)G.count();
+  }
+  const size_t exp_bytes = (4 * nexp + 255) / 256 * 256;
+  size_t ws = 0;
+  for (Group& G : P->groups) {
+    if (G.kernel != MUON_KERNEL_DENSE) continue;
     G.m_pad = round_up(G.m, kDensePad);
     G.n_pad = round_up(G.n, kDensePad);
     G.slice_ws = dense_slice_ws(G, o.mode);
     int chunk = G.count();
     if (chunk > kMaxSlicesPerLaunch) chunk = kMaxSlicesPerLaunch;
-    if (o.workspace_cap > kHeaderBytes) {
-      size_t fit = (o.workspace_cap - kHeaderBytes) / G.slice_ws;
+    if (o.workspace_cap > kHeaderBytes + exp_bytes) {
+      size_t fit = (o.workspace_cap - kHeaderBytes - exp_bytes) / G.slice_ws;
       if ((size_t)chunk > fit) chunk = fit < 1 ? 1 : (int)fit;
     } else if (o.workspace_cap > 0) {
       chunk = 1;
@@ -173,7 +182,8 @@ muon_status muon_plan(const muon_shape* shapes, int n, const muon_options* opt,
     size_t need = (size_t)chunk * G.slice_ws;
     if (need > ws) ws = need;
   }
-  P->ws_bytes = kHeaderBytes + ws;
+  P->exp_off = kHeaderBytes + ws;
+  P->ws_bytes = kHeaderBytes + ws + exp_bytes;
   } catch (const std::bad_alloc&) {
     delete P;
     return MUON_ERR_NOMEM;

@@ -87,7 +87,9 @@ muon_status step_impl(const muon_plan_t* P, void* const* params, const void* con
         st.mark(MUON_KC_SKINNY);
         e = launch_skinny(g, ptrs, ns, st, err_word, s);
       } else {
-        e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body, err_word, s, !first);
+        e = launch_dense_group_chunk(g, P->opt.mode, ptrs, ns, st, body,
+                                     reinterpret_cast<int*>(ws + P->exp_off) + g.exp_base + c0,
+                                     err_word, s, !first);
       }
       if (e != cudaSuccess) return MUON_ERR_CUDA;
       first = false;

@@ -51,6 +51,8 @@ struct TcParams {
   int has_d2;          // second fp16 output D2
   float alpha, diag;   // D  = alpha  * acc + diag  * I
   float alpha2, diag2; // D2 = alpha2 * acc + diag2 * I
+  const char* alpha_base;   // optional per-slice factor of alpha and alpha2
+  size_t alpha_stride;
   int sym;
   int b_mn;
   uint32_t idesc;      // M = 128, N = 256
@@ -320,6 +322,12 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
   const int cbytes = (p.d_f32 ? 4096 : 2048) * (p.sym ? 2 : 1) * (p.has_d2 ? 2 : 1);
   const int nbuf = EPI_BYTES / cbytes;
   const int row = row0 + lane;
+  float al = p.alpha, al2 = p.alpha2;
+  if (p.alpha_base) {
+    const float f = *reinterpret_cast<const float*>(p.alpha_base + (size_t)b * p.alpha_stride);
+    al *= f;
+    al2 *= f;
+  }
   #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     const int col0 = J * BN + c * 32;
@@ -333,8 +341,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
     #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const float d = (dg && col0 + j == row) ? 1.f : 0.f;
-      v2[j] = fmaf(p.alpha2, v[j], d * p.diag2);
-      v[j] = fmaf(p.alpha, v[j], d * p.diag);
+      v2[j] = fmaf(al2, v[j], d * p.diag2);
+      v[j] = fmaf(al, v[j], d * p.diag);
     }
     if (p.fuse) {
       float* tile = reinterpret_cast<float*>(epi_slot);
@@ -1003,6 +1011,8 @@ cudaError_t tc_gemm(const TcGemm& g, cudaStream_t s) {
   }
   p.alpha = g.alpha; p.diag = g.diag;
   p.alpha2 = g.alpha2; p.diag2 = g.diag2;
+  p.alpha_base = static_cast<const char*>(g.alpha_base);
+  p.alpha_stride = g.alpha_stride;
   p.sym = g.sym; p.b_mn = g.b_mn;
   p.idesc = pair ? tc_idesc_f16(256, BN, g.b_mn) : tc_idesc_f16(BM, BN, g.b_mn);
   p.idesc128 = tc_idesc_f16(BM, 128, g.b_mn);

@@ -30,6 +30,10 @@ struct TcGemm {
   int d_f32 = 0;
   float alpha = 1.f, diag = 0.f;
   float alpha2 = 1.f, diag2 = 0.f;
+  // optional per-slice factor of alpha and alpha2: the float at
+  // alpha_base + b * alpha_stride (device) multiplies both for slice b
+  const void* alpha_base = nullptr;
+  size_t alpha_stride = 0;
   int sym = 0;
   int b_mn = 0;
   // fused parameter update (non-symmetric products only): with W set, the

@@ -203,10 +203,13 @@ def test_workspace_cap_chunks_dense_groups(muon):
     full = muon.Plan(shapes)
     (g,) = full.groups()
     assert g["kernel"] == muon.KERNEL_DENSE and g["chunk"] == 4
-    per = (full.workspace_bytes - 256) // 4
-    capped = muon.Plan(shapes, workspace_cap=256 + 2 * per)
+    # header, chunk x slice workspace, then one exponent slot per dense slice
+    # (4 slots, padded to 256 bytes)
+    exp_region = 256
+    per = (full.workspace_bytes - 256 - exp_region) // 4
+    capped = muon.Plan(shapes, workspace_cap=256 + 2 * per + exp_region)
     assert capped.groups()[0]["chunk"] == 2
-    assert capped.workspace_bytes == 256 + 2 * per
+    assert capped.workspace_bytes == 256 + 2 * per + exp_region
     assert capped.launches(5) == 2 * full.launches(5)
 
 

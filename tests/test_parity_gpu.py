@@ -175,8 +175,9 @@ def test_chunked_workspace_gives_same_bits():
     shapes = [(5, 200, 150)]
     W, Gs, M = make_inputs(shapes, torch.bfloat16)
     full = m.Plan([(shapes[0], torch.bfloat16)])
-    per = (full.workspace_bytes - 256) // 5
-    capped = m.Plan([(shapes[0], torch.bfloat16)], workspace_cap=256 + 2 * per)
+    exp_region = 256   # one exponent slot per dense slice, padded to 256 bytes
+    per = (full.workspace_bytes - 256 - exp_region) // 5
+    capped = m.Plan([(shapes[0], torch.bfloat16)], workspace_cap=256 + 2 * per + exp_region)
     assert capped.groups()[0]["chunk"] == 2
     res = []
     for plan in (full, capped):
@@ -184,6 +185,35 @@ def test_chunked_workspace_gives_same_bits():
         O = gpu_step(plan, Wd, [Gs[0][0].cuda()], Md, HP)
         res.append((Wd[0], Md[0], O[0]))
     assert all(torch.equal(a, b) for a, b in zip(*res))
+
+
+@pytest.mark.parametrize("ortho", [True, False], ids=["O", "fused"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_first_iterate_scale_prediction_does_not_change_the_bits(dtype, ortho):
+    # The dense path writes its first iterate as fp16(V 2^-e) with e predicted
+    # from the workspace's previous step of the plan, and rewrites the slices
+    # whose prediction missed.  A zeroed workspace (every prediction misses),
+    # the same workspace again (every prediction holds) and one filled with
+    # random bytes must give the same parameters, momenta and O, bit for bit.
+    m = muon()
+    shapes = [(3, 200, 150), (300, 200), (130, 260), (2, 256, 640)]
+    W, Gs, M = make_inputs(shapes, dtype)
+    plan = m.Plan([(s, dtype) for s in shapes])
+    ws = m.alloc_workspace(plan)
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    noise = torch.randint(-128, 128, (plan.workspace_bytes,), dtype=torch.int8, device="cuda",
+                          generator=gen).view(torch.uint8)
+    res = []
+    for k in range(3):
+        if k == 2:
+            ws.copy_(noise)
+            ws[:256].zero_()   # the header's error word must read zero
+        Wd = [w.cuda() for w in W]; Md = [x.cuda() for x in M]
+        O = gpu_step(plan, Wd, [g.cuda() for g in Gs[0]], Md, HP, ortho=ortho, ws=ws)
+        res.append((Wd, Md, O if ortho else []))
+    for k in (1, 2):
+        for a, b in zip(res[0], res[k]):
+            assert all(torch.equal(x, y) for x, y in zip(a, b)), k
 
 
 def test_skinny_and_dense_paths_agree():
