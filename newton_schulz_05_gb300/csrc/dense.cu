@@ -566,8 +566,9 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
 
 }  // namespace
 
-// front, finalize, normalize, 3 products per NS step, epilogue; in the
-// tensor-core mode the last product applies the update (no epilogue launch)
+// front, finalize, then the redo pass (fp16 iterates, T > 0) or normalize,
+// 3 products per NS step, epilogue; in the tensor-core mode the last
+// product applies the update (no epilogue launch)
 int dense_launches(int ns_steps, int mode, int tr) {
   (void)tr;
   return (mode == MUON_MODE_TC16 && ns_steps > 0 ? 3 : 4) + 3 * ns_steps;
