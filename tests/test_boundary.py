@@ -354,3 +354,18 @@ def test_skinny_plans_fit_the_cluster_tensor_memory(muon):
     # a slice too long for 8 CTAs goes to the dense path
     (g,) = muon.Plan([((64, 1 << 20), torch.bfloat16)]).groups()
     assert g["kernel"] == muon.KERNEL_DENSE
+
+
+def test_alloc_host_errors_on_the_host(muon):
+    # no element, or (on a machine without a device) a registration the
+    # driver refuses: an error, and nothing is held
+    import torch
+    with pytest.raises(ValueError):
+        muon.alloc_host(0, torch.float32)
+    if not torch.cuda.is_available():
+        with pytest.raises(muon.MuonError) as e:
+            muon.alloc_host(1024, torch.float32)
+        assert e.value.status == -5
+    L = muon.load()
+    assert L.muon_host_free(None) == 0
+    assert L.muon_host_free(ctypes.c_void_p(0x123000)) == -1
