@@ -216,6 +216,17 @@ def test_first_iterate_scale_prediction_does_not_change_the_bits(dtype, ortho):
             assert all(torch.equal(x, y) for x, y in zip(a, b)), k
 
 
+@pytest.mark.parametrize("log2_scale", [-12, 40])
+def test_dense_path_gradient_scale_extremes(log2_scale):
+    # The dense path stores its first iterate as fp16(V 2^-e), e taken from
+    # ||V||.  Gradients far from unit scale (std 1e-2 times 2^-12 or 2^40; ||V||
+    # stays far above eps) must meet neither fp16 overflow nor a flush to zero:
+    # the oracle's O, element-wise parameters and momenta.
+    plan = run_and_check([(300, 200), (2, 256, 640)], torch.bfloat16, HP,
+                         grad_std=1e-2 * 2.0 ** log2_scale)
+    assert all(g["kernel"] == muon().KERNEL_DENSE for g in plan.groups())
+
+
 def test_skinny_and_dense_paths_agree():
     # the same skinny group through the fused kernel and through the dense
     # GEMM path: both within tolerance of the oracle and of each other
