@@ -49,6 +49,7 @@ struct ScaleSlot {
   int e;        // exponent of X~ = fp16(V 2^-e)
 };
 constexpr int kExpMin = -100, kExpMax = 100;   // 2^-e stays a finite fp32
+constexpr int kRedoBlocks = 148;               // blocks per slice of the redo pass
 
 struct DenseBufs {
   float* V;        // [m_pad, n_pad] fp32: front output, then O
@@ -113,8 +114,6 @@ __global__ void __launch_bounds__(kNT) front_kernel(
   }
   const float xs = ldexpf(1.f, -e);   // exact power of two
   const int tiles_c = (int)(n_pad / kFrontTileC);
-  const int64_t i0 = (int64_t)(blockIdx.x / tiles_c) * kFrontTileR;
-  const int64_t k0 = (int64_t)(blockIdx.x % tiles_c) * kFrontTileC;
   float* V = reinterpret_cast<float*>(base + off_V);
   __half* X = reinterpret_cast<__half*>(base + off_X);
   float* part = reinterpret_cast<float*>(base + off_part);
@@ -139,71 +138,86 @@ __global__ void __launch_bounds__(kNT) front_kernel(
     if (OUT == kOutV) V[w] = v;
     else X[w] = __float2half_rn(v * xs);
   };
-  if (!tr && vec) {
-    // working (i, k) = stored (i, k); 4 consecutive elements per thread
-    for (int r = warp; r < kFrontTileR; r += kNT / 32) {
-      const int64_t i = i0 + r;
-      const int64_t k = k0 + 4 * lane;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (i < m && k < n) {
-        const int64_t idx = i * n + k;
-        float g[4], mo[4];
-        load4(G + idx, g);
-        const float4 mm4 = *reinterpret_cast<const float4*>(Mo + idx);
-        mo[0] = mm4.x; mo[1] = mm4.y; mo[2] = mm4.z; mo[3] = mm4.w;
-        #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          g[q] *= gscale;
-          if (OUT != kOutRedo) mo[q] = fmaf(beta, mo[q], g[q]);
-          v[q] = nesterov ? fmaf(beta, mo[q], g[q]) : mo[q];
-          ss = fmaf(v[q], v[q], ss);
-        }
-        if (OUT != kOutRedo)
-          *reinterpret_cast<float4*>(Mo + idx) = make_float4(mo[0], mo[1], mo[2], mo[3]);
-      }
-      if (OUT == kOutV) {
-        *reinterpret_cast<float4*>(V + i * n_pad + k) = make_float4(v[0], v[1], v[2], v[3]);
-      } else {
-        __half2 a = __floats2half2_rn(v[0] * xs, v[1] * xs), b = __floats2half2_rn(v[2] * xs, v[3] * xs);
-        uint2 u;
-        u.x = *reinterpret_cast<uint32_t*>(&a);
-        u.y = *reinterpret_cast<uint32_t*>(&b);
-        *reinterpret_cast<uint2*>(X + i * n_pad + k) = u;
-      }
-    }
-  } else if (!tr) {
-    // working (i, k) = stored (i, k); stored slice is [m, n]
-    for (int r = warp; r < kFrontTileR; r += kNT / 32) {
-      const int64_t i = i0 + r;
-      for (int c = lane; c < kFrontTileC; c += 32) {
-        const int64_t k = k0 + c;
-        float v = 0.f;
+  // one tile of the working layout, tile index bt
+  auto do_tile = [&](int bt) {
+    const int64_t i0 = (int64_t)(bt / tiles_c) * kFrontTileR;
+    const int64_t k0 = (int64_t)(bt % tiles_c) * kFrontTileC;
+    if (!tr && vec) {
+      // working (i, k) = stored (i, k); 4 consecutive elements per thread
+      for (int r = warp; r < kFrontTileR; r += kNT / 32) {
+        const int64_t i = i0 + r;
+        const int64_t k = k0 + 4 * lane;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
         if (i < m && k < n) {
           const int64_t idx = i * n + k;
+          float g[4], mo[4];
+          load4(G + idx, g);
+          const float4 mm4 = *reinterpret_cast<const float4*>(Mo + idx);
+          mo[0] = mm4.x; mo[1] = mm4.y; mo[2] = mm4.z; mo[3] = mm4.w;
+          #pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            g[q] *= gscale;
+            if (OUT != kOutRedo) mo[q] = fmaf(beta, mo[q], g[q]);
+            v[q] = nesterov ? fmaf(beta, mo[q], g[q]) : mo[q];
+            ss = fmaf(v[q], v[q], ss);
+          }
+          if (OUT != kOutRedo)
+            *reinterpret_cast<float4*>(Mo + idx) = make_float4(mo[0], mo[1], mo[2], mo[3]);
+        }
+        if (OUT == kOutV) {
+          *reinterpret_cast<float4*>(V + i * n_pad + k) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+          __half2 a = __floats2half2_rn(v[0] * xs, v[1] * xs), b = __floats2half2_rn(v[2] * xs, v[3] * xs);
+          uint2 u;
+          u.x = *reinterpret_cast<uint32_t*>(&a);
+          u.y = *reinterpret_cast<uint32_t*>(&b);
+          *reinterpret_cast<uint2*>(X + i * n_pad + k) = u;
+        }
+      }
+    } else if (!tr) {
+      // working (i, k) = stored (i, k); stored slice is [m, n]
+      for (int r = warp; r < kFrontTileR; r += kNT / 32) {
+        const int64_t i = i0 + r;
+        for (int c = lane; c < kFrontTileC; c += 32) {
+          const int64_t k = k0 + c;
+          float v = 0.f;
+          if (i < m && k < n) {
+            const int64_t idx = i * n + k;
+            v = step(to_f(G[idx]) * gscale, idx);
+          }
+          ss = fmaf(v, v, ss);
+          put(i * n_pad + k, v);
+        }
+      }
+    } else {
+      // working (i, k) = stored (k, i); stored slice is [n, m]
+      for (int c = warp; c < kFrontTileC; c += kNT / 32) {
+        const int64_t k = k0 + c;
+        const int64_t i = i0 + lane;
+        float v = 0.f;
+        if (i < m && k < n) {
+          const int64_t idx = k * m + i;
           v = step(to_f(G[idx]) * gscale, idx);
         }
         ss = fmaf(v, v, ss);
-        put(i * n_pad + k, v);
+        tile[c][lane] = v;
       }
+      __syncthreads();
+      for (int r = warp; r < kFrontTileR; r += kNT / 32)
+        for (int c = lane; c < kFrontTileC; c += 32) put((i0 + r) * n_pad + k0 + c, tile[c][r]);
     }
+  };
+  if constexpr (OUT == kOutRedo) {
+    // few blocks per slice, each walking the tiles of a mispredicted slice
+    const int ntiles = (int)(m_pad / kFrontTileR) * tiles_c;
+    for (int bt = blockIdx.x; bt < ntiles; bt += gridDim.x) {
+      do_tile(bt);
+      if (tr) __syncthreads();   // the next tile reuses tile[][]
+    }
+    return;
   } else {
-    // working (i, k) = stored (k, i); stored slice is [n, m]
-    for (int c = warp; c < kFrontTileC; c += kNT / 32) {
-      const int64_t k = k0 + c;
-      const int64_t i = i0 + lane;
-      float v = 0.f;
-      if (i < m && k < n) {
-        const int64_t idx = k * m + i;
-        v = step(to_f(G[idx]) * gscale, idx);
-      }
-      ss = fmaf(v, v, ss);
-      tile[c][lane] = v;
-    }
-    __syncthreads();
-    for (int r = warp; r < kFrontTileR; r += kNT / 32)
-      for (int c = lane; c < kFrontTileC; c += 32) put((i0 + r) * n_pad + k0 + c, tile[c][r]);
+    do_tile(blockIdx.x);
   }
-  if (OUT == kOutRedo) return;
   const float tot = block_sum<kNT>(ss, red);
   if (threadIdx.x == 0) part[blockIdx.x] = tot;
 }
@@ -379,8 +393,8 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   // (X~ = fp16(V 2^-e), see the header), and a second front pass fixes the
   // slices whose exponent was mispredicted; otherwise V, then X0 = s V
   const bool spec = sizeof(IT) == 2 && st.T > 0;
-  auto front = [&](auto kern, bool pdl) {
-    return launch_k(kern, fgrid, dim3(kNT), 0, s, pdl, ptrs, g.m, g.n, mp, np, (int)g.tr, vec,
+  auto front = [&](auto kern, bool pdl, dim3 grid) {
+    return launch_k(kern, grid, dim3(kNT), 0, s, pdl, ptrs, g.m, g.n, mp, np, (int)g.tr, vec,
                     st.beta, st.nesterov, st.gscale, st.skip, (const int*)err_word, ws, sws,
                     off.V, off.X0, off.part, off.inv, (const int*)exps);
   };
@@ -392,11 +406,11 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
     NvtxRange r("muon::front_kernel");
     st.mark(MUON_KC_FRONT);
     if (spec)
-      le = bf ? front(front_kernel<__nv_bfloat16, kOutX>, pdl_first)
-              : front(front_kernel<float, kOutX>, pdl_first);
+      le = bf ? front(front_kernel<__nv_bfloat16, kOutX>, pdl_first, fgrid)
+              : front(front_kernel<float, kOutX>, pdl_first, fgrid);
     else
-      le = bf ? front(front_kernel<__nv_bfloat16, kOutV>, pdl_first)
-              : front(front_kernel<float, kOutV>, pdl_first);
+      le = bf ? front(front_kernel<__nv_bfloat16, kOutV>, pdl_first, fgrid)
+              : front(front_kernel<float, kOutV>, pdl_first, fgrid);
   }
   if (le != cudaSuccess) return le;
   {
@@ -409,8 +423,9 @@ cudaError_t run_dense(const Group& g, int mode, const SlicePtrs& ptrs, int ns,
   if (spec) {
     NvtxRange r("muon::front_kernel redo");
     st.mark(MUON_KC_NORM);
-    le = bf ? front(front_kernel<__nv_bfloat16, kOutRedo>, true)
-            : front(front_kernel<float, kOutRedo>, true);
+    const dim3 rgrid(nblk < kRedoBlocks ? nblk : kRedoBlocks, ns);
+    le = bf ? front(front_kernel<__nv_bfloat16, kOutRedo>, true, rgrid)
+            : front(front_kernel<float, kOutRedo>, true, rgrid);
   } else {
     const int64_t cnt = mp * np;
     int nb = (int)((cnt / 4 + kNT - 1) / kNT);
